@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark: one decode step (reshape_and_cache + paged decode attention) of a
+synthetic batch, timed on the GPU with CUDA events.
+
+Default workload: the GQA 8B-shaped batch (256 sequences, 32 query / 8 kv
+heads, head_dim 128, bf16, block size 16, context lengths lognormal with
+median 1000 clipped to [16, 8192]).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 0-4]
+                  [--split P] [--impl ours|reference] [--no-cpu-baseline]
+
+Under torchrun (N > 1) each rank runs its own independently seeded batch
+(replicas: sequences are independent, no data exchange); rank 0 prints the
+aggregate over all ranks with the time of the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_230_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, help="0 tiny, 1 mha7b, 2 gqa8b, 3 long_split, 4 prefix_fp8")
+    ap.add_argument("--split", type=int, default=-1, help="partition size (0 = single pass; -1 = workload default)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (barrier and max over ranks only)
+# --------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _has_cuda() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def _has_cuda():
+    import torch
+    return torch.cuda.is_available()
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device=None) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, x: float, device=None) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# roofline helpers
+# --------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_230_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, valid
+    only while the kernel sources hash to the value recorded with it."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.txt" % (kernel, workload))
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in text.splitlines():
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline object)
+# --------------------------------------------------------------------------
+
+def oracle_sample_time(wl: W.Workload, budget_s: float = 20.0):
+    """Times the oracle (scatter + decode, all host threads) on a bounded sample
+    of the batch: whole sequences in order until about `budget_s` of wall time
+    has been spent; returns (seconds, kv_bytes, seqs, threads)."""
+    import oracle
+    threads = oracle.max_threads()
+    if wl.kv_dtype == W.FP8:
+        kc = np.zeros(wl.cache_shape(), np.uint8)
+        vc = np.zeros(wl.cache_shape(), np.uint8)
+        oracle.reshape_and_cache(wl.prefill_key, wl.prefill_value, wl.q_dtype, kc, vc, "fp8", wl.prefill_slots,
+                                 wl.kv_scale)
+    else:
+        kc, vc = wl.k_cache, wl.v_cache
+    total_t, total_b, nseq = 0.0, 0, 0
+    order = np.arange(wl.S)
+    chunk = max(1, wl.S // 16)
+    i = 0
+    while i < wl.S and total_t < budget_s:
+        sel = order[i:i + chunk]
+        sub = W.subset(wl, sel)
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(sub.key, sub.value, sub.q_dtype, kc, vc, sub.kv_dtype, sub.slot_mapping,
+                                 sub.kv_scale)
+        oracle.decode(sub.q, sub.q_dtype, kc, vc, sub.kv_dtype, sub.block_tables, sub.context_lens, sub.scale,
+                      sub.kv_scale, partition_size=sub.partition_size, num_threads=threads)
+        total_t += time.perf_counter() - t0
+        total_b += sub.kv_bytes()
+        nseq += len(sel)
+        i += chunk
+    return total_t, total_b, nseq, threads
+
+
+def run_reference(args, wl, world, rank, pg):
+    if rank != 0:
+        return
+    steps = max(1, args.steps)
+    per_step = max(2.0, 60.0 / steps)
+    secs, byts, nseq = 0.0, 0, 0
+    threads = 1
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample_time(wl, budget_s=0.5)
+    for _ in range(steps):
+        t, b, n, threads = oracle_sample_time(wl, budget_s=per_step)
+        secs += t
+        byts += b
+        nseq += n
+    gbs = byts / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
+                   "head_dim": wl.D, "block_size": wl.bs, "kv_dtype": wl.kv_dtype},
+        "decode_tokens_per_s": nseq / secs,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "fp64 C oracle (scatter + decode) over leading sequences of the batch, "
+                                   "about %.0f s per step, %d sequences in total" % (per_step, nseq)},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_ours(args, wl, world, rank, local, pg):
+    import torch
+    from paged_kv_cache_230_gb300 import build as _build
+    _build.build()
+    from paged_kv_cache_230_gb300 import pagedattn as pa
+    from paged_kv_cache_230_gb300.device import DeviceBatch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    P = wl.partition_size if args.split < 0 else args.split
+    b = DeviceBatch(wl, dev, partition_size=P)
+    stream = torch.cuda.current_stream(dev)
+    kv_bytes = wl.kv_bytes()
+    alg_bytes = wl.algorithmic_bytes()
+    flush = None
+    unique_bytes = int(wl.notes.get("unique_blocks", 0)) * wl.Hkv * wl.bs * wl.D * 2 * W.ELEM_BYTES[wl.kv_dtype]
+    if unique_bytes < 4 * L2_BYTES:
+        flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        b.step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        b.scatter()
+        e1.record(stream)
+        b.decode()
+        e2.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+    dec_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    sc_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    total_ms = sum(step_ms)
+    total_ms_max = max_over_ranks(pg, total_ms, dev)
+    units = sum_over_ranks(pg, float(kv_bytes), dev)
+    seqs = sum_over_ranks(pg, float(wl.S), dev)
+    ms_per_step = total_ms_max / K
+    value = units / (ms_per_step * 1e-3) / 1e9
+    dec_avg = sum(dec_ms) / K
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
+    kernel_name = "decode_split" if P else "decode"
+    traffic = recorded_traffic(wl.name, kernel_name)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(b, wl, dev, K=min(K, 200), warm=3, pg=pg)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        t, byts, nseq, threads = oracle_sample_time(wl, budget_s=15.0)
+        cpu = {"value": byts / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": "fp64 C oracle (scatter + decode) on the first %d of %d sequences of the same batch "
+                         "(%.2f GB of KV), %.1f s" % (nseq, wl.S, byts / 1e9, t)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.q_dtype == "bf16" and wl.kv_dtype != W.FP8 else
+                     ("e4m3-kv/bf16" if wl.kv_dtype == W.FP8 else "f16"),
+            "data": "synthetic",
+            "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
+                       "head_dim": wl.D, "block_size": wl.bs, "kv_dtype": wl.kv_dtype,
+                       "context_tokens": int(wl.context_lens.sum()), "max_context": wl.max_context_len,
+                       "kv_bytes_per_step": kv_bytes, "partition_size": P,
+                       "l2": "inputs larger than L2" if flush is None else "256 MiB L2 flush between steps",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "decode_tokens_per_s": seqs / (ms_per_step * 1e-3),
+            "pct_of_hbm_peak": 100.0 * value / peak,
+            "decode_kernel_us": 1e3 * dec_avg,
+            "decode_kernel_us_median": 1e3 * statistics.median(dec_ms),
+            "scatter_us": 1e3 * sum(sc_ms) / K,
+            "wall_s": wall,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                         "kernel": "pa_" + kernel_name, "algorithmic_bytes_per_launch": alg_bytes},
+            "gpu_launches": K * b.launches_per_step(),
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def e2e_measure(b, wl, dev, K, warm, pg):
+    """Same step through the public API with inputs in pinned host memory: the
+    host->device copies of this step's q, new K/V rows, block tables, context
+    lengths and slot ids, the scatter + decode, and the device->host copy of
+    the output are all inside the timed region."""
+    import torch
+    host = {}
+    for name in ("q", "key", "value", "block_tables", "context_lens", "slot_mapping"):
+        t = getattr(b, name)
+        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    out_h = torch.empty(b.out.shape, dtype=b.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for name, t in host.items():
+            getattr(b, name).copy_(t, non_blocking=True)
+        b.step()
+        out_h.copy_(b.out, non_blocking=True)
+
+    for _ in range(warm):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1), dev) / K
+    units = sum_over_ranks(pg, float(wl.kv_bytes()), dev)
+    return {"value": units / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+
+
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup()
+    if args.impl == "reference" and rank != 0:
+        return
+    seed = args.config + 1000 * rank  # replicas draw independent batches
+    wl = W.make_config(args.config, seed=seed)
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank, pg)
+    else:
+        run_ours(args, wl, world, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

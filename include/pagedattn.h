@@ -1,0 +1,178 @@
+/*
+ * pagedattn.h: C ABI of the GB300 (sm_103a) paged KV-cache decode attention
+ * library, libpagedattn.so.
+ *
+ * The operations follow the paging scheme described for vLLM's PagedAttention
+ * (web page "vllm-project-vllm" review, §3 Q2, §6 "KV Cache Block Tables",
+ * §7): keys and values live in a pool of fixed-size physical blocks; each
+ * sequence owns a block table mapping its logical block j to a physical block
+ * id, so its blocks need not be contiguous and may be shared by several
+ * sequences (prefix / copy-on-write sharing); every decode step appends one
+ * token per sequence and attends one query token per sequence over the whole
+ * cached context, which makes the step memory-bandwidth bound.
+ *
+ * Conventions shared by every call
+ *  - All array arguments are DEVICE pointers to contiguous row-major data
+ *    owned by the caller.  The library never allocates, frees or copies
+ *    caller memory, never synchronises the stream (except in check mode, see
+ *    pa_set_check_mode) and enqueues its kernels on `stream`.
+ *  - Caches: k_cache and v_cache are [num_blocks, num_kv_heads, block_size,
+ *    head_dim] of the cache dtype, described by one pa_cache_desc.  Both must
+ *    start on a 16-byte boundary.
+ *  - Token i of sequence s is in physical block block_tables[s][i / block_size]
+ *    at offset i % block_size.  Query head g reads kv head g / G with
+ *    G = num_q_heads / num_kv_heads (contiguous grouping).
+ *  - context_lens[s] counts every cached token of sequence s including the one
+ *    written this step; entries of block_tables past ceil(context_lens[s] /
+ *    block_size) are never read.  A context length of 0 gives a zero output.
+ *  - FP8 caches use OCP E4M3 with one per-tensor scale: stored =
+ *    e4m3_rne_satfinite(x / kv_scale), read back as stored * kv_scale.  For
+ *    16-bit caches kv_scale must be 1.
+ *  - Supported: head_dim 64 or 128; block_size 8, 16 or 32; G from 1 to 16;
+ *    q/out dtype f16 or bf16; cache dtype equal to the q dtype or FP8 E4M3.
+ *  - Errors are return codes (pa_status); nothing is thrown across the ABI.
+ *    Arguments are checked on the host before anything is launched; a failed
+ *    check launches nothing.  Index values in device arrays are not read by
+ *    the host.  The kernels never access memory outside the arrays for any
+ *    index values: a block id outside the pool reads zeros, a context length
+ *    above max_blocks_per_seq * block_size is clamped, a slot outside the pool
+ *    is skipped; each such event is recorded in a device error word that
+ *    pa_get_device_error() returns, and that check mode turns into
+ *    PA_ERR_BAD_INDEX.
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer          */
+    PA_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, block_size, G, dtype  */
+    PA_ERR_WORKSPACE = -3,   /* split workspace missing or too small                 */
+    PA_ERR_CUDA = -4,        /* a CUDA runtime/driver call or launch failed          */
+    PA_ERR_BAD_INDEX = -5,   /* check mode: a kernel saw an out-of-range index       */
+    PA_ERR_TIMEOUT = -6      /* a kernel gave up waiting on its own copy pipeline    */
+} pa_status;
+
+/* Device error word bits (pa_get_device_error). */
+#define PA_DEVERR_BLOCK_ID 0x1    /* block id outside [0, num_blocks)                 */
+#define PA_DEVERR_CONTEXT_LEN 0x2 /* context length < 0 or above the table/partitions */
+#define PA_DEVERR_SLOT 0x4        /* slot id outside [0, num_blocks * block_size)     */
+#define PA_DEVERR_TIMEOUT 0x8     /* a pipeline wait ran out (about one second)       */
+
+typedef struct {
+    int64_t num_blocks;   /* physical blocks in the pool (NB)                 */
+    int32_t block_size;   /* tokens per block (8, 16 or 32)                   */
+    int32_t num_kv_heads; /* Hkv                                              */
+    int32_t head_dim;     /* D (64 or 128)                                    */
+    int32_t kv_dtype;     /* pa_dtype of both caches                          */
+} pa_cache_desc;
+
+/*
+ * pa_reshape_and_cache: writes this step's new K and V rows into the cache
+ * slots named by slot_mapping (blocks are extended each decode step, review
+ * §6 "KV Cache Block Tables").
+ *   key, value    [num_tokens, num_kv_heads, head_dim] of in_dtype (f16/bf16),
+ *                 16-byte aligned
+ *   slot_mapping  int64 [num_tokens]; slot = block * block_size + offset;
+ *                 a negative slot skips the token (padding)
+ *   k_cache/v_cache, cache   the pool (cache->kv_dtype == in_dtype, or FP8 E4M3)
+ *   kv_scale      FP8 per-tensor scale (> 0); must be 1 for 16-bit caches
+ * 16-bit caches receive a bit-exact copy.  FP8 caches receive
+ * e4m3_rne_satfinite(float(x) / kv_scale) with an IEEE float32 division.
+ * Two tokens naming the same slot in one call leave either row there.
+ */
+PA_API int pa_reshape_and_cache(const void *key, const void *value, int32_t in_dtype, int32_t num_tokens,
+                         void *k_cache, void *v_cache, const pa_cache_desc *cache,
+                         const int64_t *slot_mapping, float kv_scale, pa_stream_t stream);
+
+/*
+ * pa_decode: one query token per sequence attends over its whole paged
+ * context (review §7: decode reads the full KV cache per layer):
+ *   out[s][g] = sum_i softmax_i(scale * q[s][g] . k_i) v_i,  i < context_lens[s]
+ *   out           [num_seqs, num_q_heads, head_dim] of q_dtype (written)
+ *   q             [num_seqs, num_q_heads, head_dim] of q_dtype; q and out 16-byte aligned
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens  int32 [num_seqs]
+ *   scale         softmax scale (typically 1/sqrt(head_dim)); kv_scale as above
+ * One CTA per (sequence, kv head) streams that sequence's K/V blocks once and
+ * serves all G query heads that share them.
+ */
+PA_API int pa_decode(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+              const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+              const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+              float scale, float kv_scale, pa_stream_t stream);
+
+/*
+ * Workspace bytes pa_decode_split needs: num_seqs * num_q_heads *
+ * ceil(max_context_len / partition_size) * (head_dim + 2) * 4.  Returns 0 for
+ * invalid sizes.
+ */
+PA_API size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                      int32_t max_context_len, int32_t partition_size);
+
+/*
+ * pa_decode_split: the same result as pa_decode, computed per partition of
+ * partition_size tokens (a multiple of 64) by separate CTAs; each writes its
+ * unnormalised partial (o_p, m_p, l_p) to the workspace and a second kernel
+ * merges them by log-sum-exp:  M = max_p m_p,  L = sum_p l_p 2^(m_p - M),
+ * out = sum_p o_p 2^(m_p - M) / L  (scores kept in base 2).  Sequences with a
+ * single partition are written directly.
+ *   max_context_len  >= every context_lens[s] (the host's own bound; longer
+ *                    contexts are clamped and flagged)
+ *   workspace        device buffer of at least workspace_bytes =
+ *                    pa_decode_split_workspace_size(...), 16-byte aligned,
+ *                    owned by the caller; its contents need no initialisation
+ *                    and are scratch after the call.  Calls that share a
+ *                    workspace must be ordered on one stream.
+ */
+PA_API int pa_decode_split(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                    const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, float scale, float kv_scale,
+                    int32_t max_context_len, int32_t partition_size, void *workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/* Static description of a status code. */
+PA_API const char *pa_status_string(int status);
+
+/*
+ * Check mode (also enabled by the environment variable PA_CHECK=1 at load):
+ * every call synchronises its stream after the launch and returns
+ * PA_ERR_BAD_INDEX / PA_ERR_TIMEOUT if a kernel recorded an error.  For
+ * debugging; it is process-wide.  Returns the previous setting.
+ */
+PA_API int pa_set_check_mode(int enable);
+
+/*
+ * Synchronises the current device, returns the PA_DEVERR_* bits recorded by
+ * kernels on it since the last call, and clears them.  Returns a negative
+ * pa_status if the CUDA calls fail.
+ */
+PA_API int pa_get_device_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+PA_API int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

@@ -1,0 +1,316 @@
+// C-ABI front end of libpagedattn.so: argument checks, TMA tensor-map
+// encoding for the paged caches, launches, and the device error word.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedattn.h"
+#include "pa_internal.h"
+
+namespace {
+
+// Errors recorded by kernels (PA_DEVERR_* bits); one word per device.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
+
+int* device_error_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+std::atomic<int> g_check{-1};
+
+bool check_mode() {
+  int v = g_check.load();
+  if (v < 0) {
+    const char* e = std::getenv("PA_CHECK");
+    v = (e && e[0] && e[0] != '0') ? 1 : 0;
+    int expected = -1;
+    g_check.compare_exchange_strong(expected, v);
+    v = g_check.load();
+  }
+  return v != 0;
+}
+
+int read_and_clear_error(cudaStream_t st, bool whole_device) {
+  cudaError_t e = whole_device ? cudaDeviceSynchronize() : cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  int bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, g_device_error, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+  return bits;
+}
+
+// After a launch in check mode: wait for it and turn recorded errors into a status.
+int finish(cudaError_t launch, cudaStream_t st) {
+  if (launch != cudaSuccess) return PA_ERR_CUDA;
+  if (!check_mode()) return PA_OK;
+  const int bits = read_and_clear_error(st, false);
+  if (bits < 0) return bits;
+  if (bits & PA_DEVERR_TIMEOUT) return PA_ERR_TIMEOUT;
+  if (bits) return PA_ERR_BAD_INDEX;
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dt) { return dt == PA_FP8_E4M3 ? 1 : 2; }
+
+int check_cache(const pa_cache_desc* c, const void* k, const void* v) {
+  if (!c || !k || !v) return PA_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->num_blocks > (int64_t(1) << 32) || c->num_kv_heads <= 0 ||
+      c->num_kv_heads > 65535)
+    return PA_ERR_INVALID_ARG;
+  if (c->kv_dtype != PA_F16 && c->kv_dtype != PA_BF16 && c->kv_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+int check_kv_scale(int kv_dtype, float kv_scale) {
+  if (kv_dtype == PA_FP8_E4M3) return (std::isfinite(kv_scale) && kv_scale > 0.f) ? PA_OK : PA_ERR_INVALID_ARG;
+  return kv_scale == 1.0f ? PA_OK : PA_ERR_INVALID_ARG;
+}
+
+// ---- TMA tensor maps over [NB, Hkv, bs, D] --------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Box: one block's rows (bs) x one 128-byte (or 64-byte) slice of a row, for
+// one kv head of one block.  Coordinates (channel, offset, head, block).
+int make_cache_tensor_map(CUtensorMap* m, const void* base, const pa_cache_desc* c) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const int eb = elem_bytes(c->kv_dtype);
+  const int rowb = c->head_dim * eb;
+  const int boxb = rowb < 128 ? rowb : 128;
+  const cuuint64_t dims[4] = {cuuint64_t(c->head_dim), cuuint64_t(c->block_size), cuuint64_t(c->num_kv_heads),
+                              cuuint64_t(c->num_blocks)};
+  const cuuint64_t strides[3] = {cuuint64_t(rowb), cuuint64_t(rowb) * c->block_size,
+                                 cuuint64_t(rowb) * c->block_size * c->num_kv_heads};
+  const cuuint32_t box[4] = {cuuint32_t(boxb / eb), cuuint32_t(c->block_size), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r =
+      fn(m, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base),
+         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         boxb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  int32_t q_dtype, num_seqs, num_q_heads;
+  const void* k_cache;
+  const void* v_cache;
+  const pa_cache_desc* cache;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  float scale, kv_scale;
+};
+
+int check_decode(const DecodeArgs& a) {
+  int rc = check_cache(a.cache, a.k_cache, a.v_cache);
+  if (rc) return rc;
+  if (a.num_seqs < 0 || a.num_q_heads <= 0 || a.max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+  if (a.q_dtype != PA_F16 && a.q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (a.cache->kv_dtype != PA_FP8_E4M3 && a.cache->kv_dtype != a.q_dtype) return PA_ERR_UNSUPPORTED;
+  if (a.num_q_heads % a.cache->num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (a.num_q_heads / a.cache->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(a.scale)) return PA_ERR_INVALID_ARG;
+  rc = check_kv_scale(a.cache->kv_dtype, a.kv_scale);
+  if (rc) return rc;
+  if (static_cast<int64_t>(a.max_blocks_per_seq) * a.cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (a.num_seqs == 0) return PA_OK;
+  if (!a.out || !a.q || !a.block_tables || !a.context_lens) return PA_ERR_INVALID_ARG;
+  if (!aligned16(a.out) || !aligned16(a.q)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+pa::DecodeParams make_params(const DecodeArgs& a, int* err) {
+  pa::DecodeParams p{};
+  p.out = a.out;
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.err = err;
+  p.num_blocks = a.cache->num_blocks;
+  p.S = a.num_seqs;
+  p.Hq = a.num_q_heads;
+  p.Hkv = a.cache->num_kv_heads;
+  p.G = a.num_q_heads / a.cache->num_kv_heads;
+  p.bs = a.cache->block_size;
+  p.maxB = a.max_blocks_per_seq;
+  p.q_dtype = a.q_dtype;
+  p.partition_size = 0;
+  p.Pmax = 1;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.kv_scale = a.cache->kv_dtype == PA_FP8_E4M3 ? a.kv_scale : 1.0f;
+  return p;
+}
+
+cudaError_t launch_decode(const pa::DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int kv_dtype,
+                          int head_dim, cudaStream_t st) {
+  switch (kv_dtype) {
+    case PA_F16: return pa::launch_decode_f16(p, tk, tv, head_dim, st);
+    case PA_BF16: return pa::launch_decode_bf16(p, tk, tv, head_dim, st);
+    default: return pa::launch_decode_fp8(p, tk, tv, head_dim, st);
+  }
+}
+
+int64_t split_partitions(int32_t max_context_len, int32_t partition_size) {
+  if (max_context_len <= 0) return 1;
+  return (static_cast<int64_t>(max_context_len) + partition_size - 1) / partition_size;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_reshape_and_cache(const void* key, const void* value, int32_t in_dtype, int32_t num_tokens, void* k_cache,
+                         void* v_cache, const pa_cache_desc* cache, const int64_t* slot_mapping, float kv_scale,
+                         pa_stream_t stream) {
+  int rc = check_cache(cache, k_cache, v_cache);
+  if (rc) return rc;
+  if (in_dtype != PA_F16 && in_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != PA_FP8_E4M3 && cache->kv_dtype != in_dtype) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  rc = check_kv_scale(cache->kv_dtype, kv_scale);
+  if (rc) return rc;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value)) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  pa::CacheParams p{};
+  p.key = key;
+  p.value = value;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.slot_mapping = slot_mapping;
+  p.err = err;
+  p.num_blocks = cache->num_blocks;
+  p.T = num_tokens;
+  p.Hkv = cache->num_kv_heads;
+  p.D = cache->head_dim;
+  p.bs = cache->block_size;
+  p.in_dtype = in_dtype;
+  p.cache_dtype = cache->kv_dtype;
+  p.kv_scale = cache->kv_dtype == PA_FP8_E4M3 ? kv_scale : 1.0f;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(pa::launch_reshape_and_cache(p, st), st);
+}
+
+int pa_decode(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
+              const void* v_cache, const pa_cache_desc* cache, const int32_t* block_tables,
+              int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, float kv_scale,
+              pa_stream_t stream) {
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, kv_scale};
+  int rc = check_decode(a);
+  if (rc || num_seqs == 0) return rc;
+  if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
+    return rc;
+  const pa::DecodeParams p = make_params(a, err);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st), st);
+}
+
+size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                      int32_t max_context_len, int32_t partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size <= 0) return 0;
+  const int64_t np = split_partitions(max_context_len, partition_size);
+  return static_cast<size_t>(num_seqs) * num_q_heads * np * (head_dim + 2) * sizeof(float);
+}
+
+int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                    const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    float scale, float kv_scale, int32_t max_context_len, int32_t partition_size, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, kv_scale};
+  int rc = check_decode(a);
+  if (rc) return rc;
+  if (partition_size <= 0 || partition_size % pa::kTileTokens || max_context_len < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  const int64_t np = split_partitions(max_context_len, partition_size);
+  if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads * np > INT32_MAX) return PA_ERR_INVALID_ARG;
+  const size_t need = pa_decode_split_workspace_size(num_seqs, num_q_heads, cache->head_dim, max_context_len,
+                                                     partition_size);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
+    return rc;
+  pa::DecodeParams p = make_params(a, err);
+  p.partition_size = partition_size;
+  p.Pmax = static_cast<int>(np);
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * np;
+  p.ws_ml = static_cast<float*>(workspace);
+  p.ws_o = p.ws_ml + rows * 2;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st);
+  if (e == cudaSuccess) e = pa::launch_lse_merge(p, cache->head_dim, st);
+  return finish(e, st);
+}
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_BAD_INDEX: return "out-of-range index seen by a kernel";
+    case PA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int pa_set_check_mode(int enable) {
+  const int prev = check_mode() ? 1 : 0;
+  g_check.store(enable ? 1 : 0);
+  return prev;
+}
+
+int pa_get_device_error(void) { return read_and_clear_error(nullptr, true); }
+
+int pa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,722 @@
+// Paged decode attention kernels for sm_103a.
+//
+// Work unit: one CTA per (sequence s, kv head h) — or per (s, h, partition)
+// in the split variant.  The CTA streams the K and V rows of its token range
+// through a ring of shared-memory stages exactly once and serves all G query
+// heads that read kv head h (decode reads the full KV cache once per step and
+// is bandwidth bound: vLLM review, §7).
+//
+//   warp 4 (producer): walks the block table (logical block j -> physical
+//     block id, review §6 "KV Cache Block Tables"), 32 entries per coalesced
+//     load, and issues one 4-D TMA tile load per (block, 128-byte segment) for
+//     K and for V into the next free stage.  TMA writes the tile with the
+//     128-byte (or 64-byte) swizzle so the consumers' row reads are free of
+//     bank conflicts.  A block id outside the pool is a TMA out-of-bounds box
+//     and reads zeros.
+//   warps 0-3 (consumers): each owns 16 consecutive tokens of every stage and
+//     keeps its own running max m, running sum l and output accumulator for
+//     the G query heads (online softmax, base 2: scores are pre-scaled by
+//     log2 e).  After the last stage the four partial states are merged in a
+//     fixed order, so the result depends only on logical token positions —
+//     never on where blocks sit in the pool or on timing.
+//
+// Group product.  For G >= 4 the per-warp work is two warp MMAs per 16 tokens
+// (m16n8k16, fp32 accumulate):  S^T[16 tok x 8 heads] = K[16 x D] Q^T and
+// O^T[D x 8 heads] += V^T[D x 16 tok] P^T, with the query group padded to 8
+// (or 16) columns.  For G <= 3 (too narrow to be a dense contraction) each
+// token row is split over 8 lanes that form dot products with warp shuffles.
+//
+// FP8 E4M3 caches: codes are widened exactly to f16 in registers and the MMA
+// runs in f16.  q is scaled by a power of two 2^e chosen per CTA so that
+// max|q| * 2^e lies in [2^14, 2^15) before its f16 rounding, which keeps the
+// f16 copy exact except for entries below 2^-29 max|q|; 2^-e and kv_scale are
+// folded into the score multiplier and kv_scale into the output.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math_constants.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kErrBlockId = 0x1;
+constexpr int kErrContextLen = 0x2;
+constexpr int kErrSlot = 0x4;
+constexpr int kErrTimeout = 0x8;
+
+template <int KV, int D>
+struct Geom {
+  static constexpr int EB = (KV == kE4M3) ? 1 : 2;         // bytes per element
+  static constexpr int ROWB = D * EB;                       // bytes per token row
+  static constexpr int BOXB = ROWB < 128 ? ROWB : 128;      // bytes per TMA box row
+  static constexpr int BOXE = BOXB / EB;                    // elements per box row
+  static constexpr int NSEG = ROWB / BOXB;                  // boxes per token row
+  static constexpr int SWZ = (BOXB == 128) ? 0x70 : 0x30;   // swizzle XOR mask (bits 4-6 / 4-5)
+  static constexpr int SEG_BYTES = kTileTokens * BOXB;
+  static constexpr int HALF_BYTES = NSEG * SEG_BYTES;       // K (or V) bytes per stage
+  static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
+  static constexpr int NST_RAW = kRingBytes / STAGE_BYTES;
+  static constexpr int NST = NST_RAW < 2 ? 2 : (NST_RAW > 8 ? 8 : NST_RAW);
+  static constexpr int RING = NST * STAGE_BYTES;
+  static_assert(SEG_BYTES % 1024 == 0, "segments must keep the swizzle atom alignment");
+};
+
+// Byte offset inside a swizzled segment: the 16-byte chunk index (bits 4-6,
+// or 4-5) is XORed with the row index bits (7-9, or 7-8), as TMA writes it.
+template <class Gm>
+__device__ __forceinline__ uint32_t swz(uint32_t off) {
+  return off ^ ((off >> 3) & Gm::SWZ);
+}
+
+template <int NG, int D>
+__host__ __device__ constexpr int decode_smem_bytes_for(int ring, int nst) {
+  return 1024 + ring + NG * D * 4 + 2 * nst * 8 + 64;
+}
+
+template <int KV, int D, int NG>
+constexpr int decode_smem_bytes() {
+  return decode_smem_bytes_for<NG, D>(Geom<KV, D>::RING, Geom<KV, D>::NST);
+}
+
+__device__ __forceinline__ float load_q(const void* q, int64_t idx, int q_dtype) {
+  const uint16_t bits = static_cast<const uint16_t*>(q)[idx];
+  return q_dtype == kF16 ? __half2float(__ushort_as_half(bits)) : __uint_as_float(uint32_t(bits) << 16);
+}
+
+__device__ __forceinline__ void store_out(void* out, int64_t idx, int q_dtype, float v) {
+  uint16_t bits = q_dtype == kF16 ? __half_as_ushort(__float2half_rn(v))
+                                  : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  static_cast<uint16_t*>(out)[idx] = bits;
+}
+
+template <bool IS_BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (IS_BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Two E4M3 codes (low byte = first element) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return uint32_t(r.x) | (uint32_t(r.y) << 16);
+}
+
+// Zero the halves of an A fragment whose token index (k) is >= n_valid.
+// a[0], a[1] hold tokens 2c, 2c+1; a[2], a[3] hold tokens 8+2c, 9+2c (c = lane % 4).
+__device__ __forceinline__ void mask_tokens(uint32_t (&a)[4], int lane, int n_valid) {
+  const int t0 = 2 * (lane & 3);
+  const uint32_t m_lo = (t0 < n_valid ? 0x0000FFFFu : 0u) | (t0 + 1 < n_valid ? 0xFFFF0000u : 0u);
+  const uint32_t m_hi = (t0 + 8 < n_valid ? 0x0000FFFFu : 0u) | (t0 + 9 < n_valid ? 0xFFFF0000u : 0u);
+  a[0] &= m_lo;
+  a[1] &= m_lo;
+  a[2] &= m_hi;
+  a[3] &= m_hi;
+}
+
+// Widen one lane's piece of a token row (PB bytes at a 16- or 8-byte aligned
+// shared address) to floats.
+template <int KV, int PB>
+__device__ __forceinline__ void load_piece(const uint8_t* src, float* f) {
+  if constexpr (PB == 16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if constexpr (KV == kF16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+      }
+    } else if constexpr (KV == kBF16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t h2 = e4m3x2_to_f16x2(w[i] >> (16 * j));
+          const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          f[4 * i + 2 * j] = v.x;
+          f[4 * i + 2 * j + 1] = v.y;
+        }
+      }
+    }
+  } else {
+    static_assert(KV == kE4M3, "8-byte pieces only occur for FP8 rows of 64 bytes");
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t h2 = e4m3x2_to_f16x2(w[i] >> (16 * j));
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        f[4 * i + 2 * j] = v.x;
+        f[4 * i + 2 * j + 1] = v.y;
+      }
+    }
+  }
+}
+
+template <int KV, int D, bool USE_MMA, int NG>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeParams p) {
+  using Gm = Geom<KV, D>;
+  constexpr int NST = Gm::NST;
+  constexpr int NCW = kConsumerWarps;
+  constexpr int TILE = kTileTokens;
+  static_assert(NCW * NG * D * 4 + 2 * NCW * NG * 4 <= Gm::RING, "merge area must fit in the ring");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+  const uint32_t ring_u32 = smem_u32(smem);
+  float* qbuf = reinterpret_cast<float*>(smem + Gm::RING);  // [NG][D]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::RING + NG * D * 4);
+  float* red = reinterpret_cast<float*>(bars + 2 * NST);     // 16 floats
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + NST * 8;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- which (sequence, kv head, partition) ----
+  int bid = blockIdx.x;
+  const int part = bid % p.Pmax;
+  bid /= p.Pmax;
+  const int h = bid % p.Hkv;
+  const int s = bid / p.Hkv;
+  const bool split = p.partition_size > 0;
+  int lmax = p.maxB * p.bs;
+  if (split) lmax = min(lmax, p.Pmax * p.partition_size);
+  int L = p.context_lens[s];
+  if (L < 0 || L > lmax) {
+    if (tid == 0 && part == 0 && h == 0) atomicOr(p.err, kErrContextLen);
+    L = min(max(L, 0), lmax);
+  }
+  int tok_begin = 0, tok_end = L;
+  if (split) {
+    tok_begin = part * p.partition_size;
+    tok_end = min(L, tok_begin + p.partition_size);
+    if (part > 0 && tok_begin >= L) return;  // partition past the end of this context
+  }
+  const bool single = !split || L <= p.partition_size;  // this CTA writes the final output
+  const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TILE - 1) / TILE : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, NCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == NCW) {
+    // ======================= producer warp =======================
+    if (ntiles == 0) return;
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int bs = p.bs;
+    const int* bt_row = p.block_tables + static_cast<int64_t>(s) * p.maxB;
+    const int blk_begin = tok_begin / bs;
+    const int blk_end = (tok_end + bs - 1) / bs;
+    const int bpt = TILE / bs;  // blocks per stage
+    const uint32_t tx = static_cast<uint32_t>(2 * bs * Gm::ROWB);
+    int base = blk_begin;
+    int cur = (base + lane < blk_end) ? __ldg(bt_row + base + lane) : -1;
+    int nxt = (base + 32 + lane < blk_end) ? __ldg(bt_row + base + 32 + lane) : -1;
+    int t = 0;
+    bool ok = true;
+    for (; t < ntiles; ++t) {
+      const int stage = t % NST;
+      if (t >= NST && !mbar_wait(empty0 + 8 * stage, ((t / NST) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int b0 = blk_begin + t * bpt;
+      const int nb = min(bpt, blk_end - b0);
+      const uint32_t full = full0 + 8 * stage;
+      if (lane == 0) mbar_arrive_expect_tx(full, tx * nb);
+      const uint32_t kdst0 = ring_u32 + stage * Gm::STAGE_BYTES;
+      for (int i = 0; i < nb; ++i) {
+        const int b = b0 + i;
+        if (b >= base + 32) {
+          base += 32;
+          cur = nxt;
+          nxt = (base + 32 + lane < blk_end) ? __ldg(bt_row + base + 32 + lane) : -1;
+        }
+        const int phys = __shfl_sync(0xFFFFFFFFu, cur, b - base);
+        if (lane == 0) {
+          if (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks) atomicOr(p.err, kErrBlockId);
+          const uint32_t kdst = kdst0 + i * bs * Gm::BOXB;
+#pragma unroll
+          for (int sg = 0; sg < Gm::NSEG; ++sg) {
+            tma_load_4d(kdst + sg * Gm::SEG_BYTES, &tmK, full, sg * Gm::BOXE, 0, h, phys);
+            tma_load_4d(kdst + Gm::HALF_BYTES + sg * Gm::SEG_BYTES, &tmV, full, sg * Gm::BOXE, 0, h, phys);
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(p.err, kErrTimeout);
+      // let the copies already issued land before the CTA can exit
+      for (int u = max(0, t - NST); u < t; ++u) mbar_wait(full0 + 8 * (u % NST), (u / NST) & 1);
+    }
+    return;
+  }
+
+  // ========================= consumer warps =========================
+  const int cw = warp;
+  const int ctid = tid;  // 0..127
+  const int qrow0 = s * p.Hq + h * p.G;
+  float qmax = 0.f;
+  for (int idx = ctid; idx < NG * D; idx += NCW * 32) {
+    const int g = idx / D, d = idx % D;
+    float v = 0.f;
+    if (g < p.G) v = load_q(p.q, static_cast<int64_t>(qrow0 + g) * D + d, p.q_dtype);
+    qbuf[idx] = v;
+    qmax = fmaxf(qmax, fabsf(v));
+  }
+  float qk_mult = p.scale_log2 * p.kv_scale;
+  float qmul = 1.f;
+  if constexpr (KV == kE4M3 && USE_MMA) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, o));
+    if (lane == 0) red[cw] = qmax;
+  }
+  named_bar_sync(1, NCW * 32);
+  if constexpr (KV == kE4M3 && USE_MMA) {
+    qmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    int e = 0;
+    if (qmax > 0.f) {
+      int ex;
+      frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
+      e = min(15 - ex, 126);
+    }
+    qmul = ldexpf(1.f, e);
+    qk_mult = ldexpf(qk_mult, -e);
+  }
+
+  const int qr = lane >> 2, qc = lane & 3;
+
+  if constexpr (USE_MMA) {
+    constexpr int NT = NG / 8;   // head tiles of 8
+    constexpr int KS = D / 16;   // 16-wide k-steps (and 16-row output tiles)
+    constexpr bool BF = (KV == kBF16);
+    uint32_t qf[KS][NT][2];
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float* qg = qbuf + (nt * 8 + qr) * D;
+        if constexpr (KV == kE4M3) {
+          const int d = 16 * j + 4 * qc;  // k order of the widened FP8 fragments
+          qf[j][nt][0] = pack2<false>(qg[d] * qmul, qg[d + 1] * qmul);
+          qf[j][nt][1] = pack2<false>(qg[d + 2] * qmul, qg[d + 3] * qmul);
+        } else {
+          const int d = 16 * j + 2 * qc;
+          qf[j][nt][0] = pack2<BF>(qg[d], qg[d + 1]);
+          qf[j][nt][1] = pack2<BF>(qg[d + 8], qg[d + 9]);
+        }
+      }
+    }
+    float m_run[NT][2], l_run[NT][2], oacc[KS][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
+    }
+    const int row0 = cw * 16;
+    for (int t = 0; t < ntiles; ++t) {
+      const int stage = t % NST;
+      if (!mbar_wait(full0 + 8 * stage, (t / NST) & 1)) {
+        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        break;
+      }
+      const int n_valid = min(16, tok_end - (tok_begin + t * TILE + row0));
+      if (n_valid > 0) {
+        const uint32_t kst = ring_u32 + stage * Gm::STAGE_BYTES;
+        const uint32_t vst = kst + Gm::HALF_BYTES;
+        float sacc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+        // ---- S^T = K Q^T ----
+        if constexpr (KV != kE4M3) {
+          const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {
+            const int cb = 32 * j;
+            const int sg = cb / Gm::BOXB, c = (cb % Gm::BOXB) / 16 + (lane >> 4);
+            uint32_t a[4];
+            ldsm_x4(kst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + c * 16), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<BF>(sacc[nt], a, qf[j][nt][0], qf[j][nt][1]);
+          }
+        } else {
+          const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int j = 0; j < KS; j += 2) {
+            const int c = j + (lane >> 4);
+            uint32_t R[4];
+            ldsm_x4(kst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              uint32_t a[4];
+              a[0] = e4m3x2_to_f16x2(R[2 * kk]);
+              a[2] = e4m3x2_to_f16x2(R[2 * kk] >> 16);
+              a[1] = e4m3x2_to_f16x2(R[2 * kk + 1]);
+              a[3] = e4m3x2_to_f16x2(R[2 * kk + 1] >> 16);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma16816<false>(sacc[nt], a, qf[j + kk][nt][0], qf[j + kk][nt][1]);
+            }
+          }
+        }
+        // ---- online softmax over this warp's 16 tokens ----
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float sv[4], alpha[2];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = qr + (e >= 2 ? 8 : 0);
+            sv[e] = row < n_valid ? sacc[nt][e] * qk_mult : -CUDART_INF_F;
+          }
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            float mx = fmaxf(sv[c2], sv[c2 + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+            const float m_new = fmaxf(m_run[nt][c2], mx);
+            const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+            alpha[c2] = ex2(m_run[nt][c2] - m_use);
+            sv[c2] = ex2(sv[c2] - m_use);
+            sv[c2 + 2] = ex2(sv[c2 + 2] - m_use);
+            l_run[nt][c2] = l_run[nt][c2] * alpha[c2] + (sv[c2] + sv[c2 + 2]);
+            m_run[nt][c2] = m_new;
+          }
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            oacc[mt][nt][0] *= alpha[0];
+            oacc[mt][nt][1] *= alpha[1];
+            oacc[mt][nt][2] *= alpha[0];
+            oacc[mt][nt][3] *= alpha[1];
+          }
+          // P^T fragment (rows = tokens) -> transposed into the B operand of the PV product
+          pb[nt][0] = movm_t(pack2<BF>(sv[0], sv[1]));
+          pb[nt][1] = movm_t(pack2<BF>(sv[2], sv[3]));
+        }
+        // ---- O^T += V^T P^T ----
+        if constexpr (KV != kE4M3) {
+          const int r = row0 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            const int cb = 32 * mt;
+            const int sg = cb / Gm::BOXB, c = (cb % Gm::BOXB) / 16 + ((lane >> 3) & 1);
+            uint32_t a[4];
+            ldsm_x4_t(vst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + c * 16), a[0], a[1], a[2], a[3]);
+            if (n_valid < 16) mask_tokens(a, lane, n_valid);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<BF>(oacc[mt][nt], a, pb[nt][0], pb[nt][1]);
+          }
+        } else {
+          const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int j = 0; j < KS; j += 2) {
+            const int c = j + (lane >> 4);
+            uint32_t R[4];
+            ldsm_x4(vst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              // rows = tokens, columns = channels; transposing the widened 8x8
+              // pieces yields V^T fragments whose 16 rows are the channels
+              // 16j' + {0,1,4,5,8,9,12,13} (low) and {2,3,6,7,10,11,14,15} (high)
+              uint32_t a[4];
+              a[0] = movm_t(e4m3x2_to_f16x2(R[2 * kk]));
+              a[1] = movm_t(e4m3x2_to_f16x2(R[2 * kk] >> 16));
+              a[2] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1]));
+              a[3] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1] >> 16));
+              if (n_valid < 16) mask_tokens(a, lane, n_valid);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma16816<false>(oacc[j + kk][nt], a, pb[nt][0], pb[nt][1]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    }
+
+    // ---- merge the four warps' partial states ----
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        float l = l_run[nt][c2];
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+        l_run[nt][c2] = l;
+      }
+    }
+    named_bar_sync(1, NCW * 32);  // every consumer is done reading the ring
+    float* os = reinterpret_cast<float*>(smem);  // [NCW][NG][D]
+    float* msb = os + NCW * NG * D;              // [NCW][NG]
+    float* lsb = msb + NCW * NG;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int g = nt * 8 + 2 * qc + (e & 1);
+          int d;
+          if constexpr (KV == kE4M3) {
+            d = 16 * mt + 4 * (qr >> 1) + (qr & 1) + (e >= 2 ? 2 : 0);
+          } else {
+            d = 16 * mt + qr + (e >= 2 ? 8 : 0);
+          }
+          os[(cw * NG + g) * D + d] = oacc[mt][nt][e];
+        }
+      }
+    }
+    if (qr == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int g = nt * 8 + 2 * qc + c2;
+          msb[cw * NG + g] = m_run[nt][c2];
+          lsb[cw * NG + g] = l_run[nt][c2];
+        }
+    }
+  } else {
+    // ================= warp-shuffle path (G <= 3) =================
+    constexpr int EPL = D / 8;              // elements per lane per row
+    constexpr int PB = Gm::BOXB / 8;        // bytes per lane per segment
+    constexpr int EPS = PB / Gm::EB;        // elements per lane per segment
+    const int grp = lane >> 3, sub = lane & 7;
+    float qv[NG][EPL];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int sg = 0; sg < Gm::NSEG; ++sg)
+#pragma unroll
+        for (int e = 0; e < EPS; ++e) qv[g][sg * EPS + e] = qbuf[g * D + sg * Gm::BOXE + sub * EPS + e];
+    float m_run[NG], l_run[NG], o[NG][EPL];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      m_run[g] = -CUDART_INF_F;
+      l_run[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[g][e] = 0.f;
+    }
+    const int row0 = cw * 16;
+    for (int t = 0; t < ntiles; ++t) {
+      const int stage = t % NST;
+      if (!mbar_wait(full0 + 8 * stage, (t / NST) & 1)) {
+        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        break;
+      }
+      const int n_valid = min(16, tok_end - (tok_begin + t * TILE + row0));
+      if (n_valid > 0) {
+        const uint8_t* kst = smem + stage * Gm::STAGE_BYTES;
+        const uint8_t* vst = kst + Gm::HALF_BYTES;
+        float sc[4][NG];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * i + grp, r = row0 + rr;
+          float kf[EPL];
+#pragma unroll
+          for (int sg = 0; sg < Gm::NSEG; ++sg)
+            load_piece<KV, PB>(kst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + sub * PB), kf + sg * EPS);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) dot = fmaf(qv[g][e], kf[e], dot);
+            dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
+            dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 2);
+            dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 4);
+            sc[i][g] = rr < n_valid ? dot * qk_mult : -CUDART_INF_F;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const float mx = fmaxf(fmaxf(sc[0][g], sc[1][g]), fmaxf(sc[2][g], sc[3][g]));
+          const float m_new = fmaxf(m_run[g], mx);
+          const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+          const float alpha = ex2(m_run[g] - m_use);
+          float lsum = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sc[i][g] = ex2(sc[i][g] - m_use);
+            lsum += sc[i][g];
+          }
+          l_run[g] = l_run[g] * alpha + lsum;
+          m_run[g] = m_new;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[g][e] *= alpha;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * i + grp, r = row0 + rr;
+          if (rr < n_valid) {
+            float vf[EPL];
+#pragma unroll
+            for (int sg = 0; sg < Gm::NSEG; ++sg)
+              load_piece<KV, PB>(vst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + sub * PB), vf + sg * EPS);
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) o[g][e] = fmaf(sc[i][g], vf[e], o[g][e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    }
+    // merge the four 8-lane groups (commutative, so every lane gets the same bits)
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const float m_o = __shfl_xor_sync(0xFFFFFFFFu, m_run[g], off);
+        const float l_o = __shfl_xor_sync(0xFFFFFFFFu, l_run[g], off);
+        const float M = fmaxf(m_run[g], m_o);
+        const float M_use = M == -CUDART_INF_F ? 0.f : M;
+        const float a = ex2(m_run[g] - M_use), b = ex2(m_o - M_use);
+        l_run[g] = l_run[g] * a + l_o * b;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float o_o = __shfl_xor_sync(0xFFFFFFFFu, o[g][e], off);
+          o[g][e] = o[g][e] * a + o_o * b;
+        }
+        m_run[g] = M;
+      }
+    }
+    named_bar_sync(1, NCW * 32);
+    float* os = reinterpret_cast<float*>(smem);
+    float* msb = os + NCW * NG * D;
+    float* lsb = msb + NCW * NG;
+    if (grp == 0) {
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+#pragma unroll
+        for (int sg = 0; sg < Gm::NSEG; ++sg)
+#pragma unroll
+          for (int e = 0; e < EPS; ++e) os[(cw * NG + g) * D + sg * Gm::BOXE + sub * EPS + e] = o[g][sg * EPS + e];
+        if (sub == 0) {
+          msb[cw * NG + g] = m_run[g];
+          lsb[cw * NG + g] = l_run[g];
+        }
+      }
+    }
+  }
+
+  // ---- final combination of the four warps, in warp order ----
+  named_bar_sync(1, NCW * 32);
+  {
+    const float* os = reinterpret_cast<const float*>(smem);
+    const float* msb = os + NCW * NG * D;
+    const float* lsb = msb + NCW * NG;
+    const float vscale = (KV == kE4M3) ? p.kv_scale : 1.f;
+    for (int idx = ctid; idx < p.G * D; idx += NCW * 32) {
+      const int g = idx / D, d = idx % D;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, msb[w * NG + g]);
+      float lsum = 0.f, acc = 0.f;
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float sc = ex2(msb[w * NG + g] - M);
+          lsum += lsb[w * NG + g] * sc;
+          acc += os[(w * NG + g) * D + d] * sc;
+        }
+      }
+      acc *= vscale;
+      const int64_t row = qrow0 + g;
+      if (single) {
+        store_out(p.out, row * D + d, p.q_dtype, lsum > 0.f ? acc / lsum : 0.f);
+      } else {
+        const int64_t slot = row * p.Pmax + part;
+        p.ws_o[slot * D + d] = acc;
+        if (d == 0) {
+          p.ws_ml[2 * slot] = M;
+          p.ws_ml[2 * slot + 1] = lsum;
+        }
+      }
+    }
+  }
+}
+
+// Log-sum-exp merge of the split partials of one (sequence, query head) per CTA.
+template <int D>
+__global__ void __launch_bounds__(D) lse_merge_kernel(const DecodeParams p) {
+  const int row = blockIdx.x;  // s * Hq + query head
+  const int s = row / p.Hq;
+  const int lmax = min(p.maxB * p.bs, p.Pmax * p.partition_size);
+  const int L = min(max(p.context_lens[s], 0), lmax);
+  const int np = (L + p.partition_size - 1) / p.partition_size;
+  if (np <= 1) return;  // written directly by its only partition
+  const int d = threadIdx.x;
+  const float* ml = p.ws_ml + static_cast<int64_t>(row) * p.Pmax * 2;
+  const float* o = p.ws_o + static_cast<int64_t>(row) * p.Pmax * D;
+  float M = -CUDART_INF_F;
+  for (int i = 0; i < np; ++i) M = fmaxf(M, ml[2 * i]);
+  float lsum = 0.f, acc = 0.f;
+  for (int i = 0; i < np; ++i) {
+    const float sc = ex2(ml[2 * i] - M);
+    lsum += ml[2 * i + 1] * sc;
+    acc += o[static_cast<int64_t>(i) * D + d] * sc;
+  }
+  store_out(p.out, static_cast<int64_t>(row) * D + d, p.q_dtype, lsum > 0.f ? acc / lsum : 0.f);
+}
+
+template <int KV, int D, bool USE_MMA, int NG>
+cudaError_t launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       cudaStream_t st) {
+  constexpr int smem = decode_smem_bytes<KV, D, NG>();
+  auto kern = decode_kernel<KV, D, USE_MMA, NG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.S) * p.Hkv * p.Pmax;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+template <int KV, int D>
+cudaError_t launch_for_d(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                         cudaStream_t st) {
+  if (p.G == 1) return launch_one<KV, D, false, 1>(p, tmK, tmV, st);
+  if (p.G <= 3) return launch_one<KV, D, false, 3>(p, tmK, tmV, st);
+  if (p.G <= 8) return launch_one<KV, D, true, 8>(p, tmK, tmV, st);
+  return launch_one<KV, D, true, 16>(p, tmK, tmV, st);
+}
+
+template <int KV>
+cudaError_t launch_decode_kv(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             int head_dim, cudaStream_t st) {
+  if (head_dim == 64) return launch_for_d<KV, 64>(p, tmK, tmV, st);
+  return launch_for_d<KV, 128>(p, tmK, tmV, st);
+}
+
+}  // namespace pa

@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI front end (pa_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;                 // warps that compute
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kTileTokens = 16 * kConsumerWarps;  // tokens per pipeline stage
+constexpr int kRingBytes = 96 * 1024;             // target bytes of the K/V stage ring
+constexpr int kMaxGroup = 16;                     // largest query group G
+
+enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+struct DecodeParams {
+  void* out;                  // [S, Hq, D] of q_dtype
+  const void* q;              // [S, Hq, D] of q_dtype
+  const int32_t* block_tables;  // [S, maxB]
+  const int32_t* context_lens;  // [S]
+  float* ws_ml;               // split: [S, Hq, Pmax, 2] (m, l); nullptr without split
+  float* ws_o;                // split: [S, Hq, Pmax, D]
+  int* err;                   // device error word (PA_DEVERR_* bits)
+  int64_t num_blocks;
+  int S, Hq, Hkv, G, bs, maxB;
+  int q_dtype;
+  int partition_size;         // tokens per partition; 0 = whole context per CTA
+  int Pmax;                   // partitions per sequence in the grid (1 without split)
+  float scale_log2;           // scale * log2(e)
+  float kv_scale;             // FP8 dequantisation scale (1 for 16-bit caches)
+};
+
+// Launches the decode (or split-partition) kernel for one cache dtype.
+// tmK/tmV: 4-D tensor maps over [NB, Hkv, bs, D] with the box and swizzle that
+// make_cache_tensor_map (pa_api.cu) chose for this cache dtype and head_dim.
+cudaError_t launch_decode_f16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              int head_dim, cudaStream_t st);
+cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               int head_dim, cudaStream_t st);
+cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              int head_dim, cudaStream_t st);
+
+// Log-sum-exp merge of split partials into out.
+cudaError_t launch_lse_merge(const DecodeParams& p, int head_dim, cudaStream_t st);
+
+struct CacheParams {
+  const void* key;
+  const void* value;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* slot_mapping;
+  int* err;
+  int64_t num_blocks;
+  int T, Hkv, D, bs;
+  int in_dtype, cache_dtype;
+  float kv_scale;
+};
+
+cudaError_t launch_reshape_and_cache(const CacheParams& p, cudaStream_t st);
+
+}  // namespace pa

@@ -1,0 +1,209 @@
+"""Python binding of libpagedattn.so (ctypes; argument marshalling only).
+
+Every function here checks tensor devices, dtypes, shapes and contiguity,
+then passes raw device pointers and the current CUDA stream to the C ABI
+declared in ``include/pagedattn.h``.  All arithmetic runs in the library's
+kernels; there is no fallback.  Importing this module loads the library and
+raises if it has not been built (``paged_kv_cache_230_gb300.build.build()``).
+
+Tensor conventions (torch, on the GPU):
+  q, out              [S, Hq, D]  float16 or bfloat16
+  key, value          [T, Hkv, D] float16 or bfloat16
+  k_cache, v_cache    [NB, Hkv, bs, D] float16 / bfloat16, or uint8 /
+                      float8_e4m3fn holding OCP E4M3 codes
+  block_tables        int32 [S, max_blocks_per_seq]
+  context_lens        int32 [S]
+  slot_mapping        int64 [T]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: "workspace",
+          -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out"}
+DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_split_workspace_size", "pa_decode_split",
+           "pa_status_string", "pa_set_check_mode", "pa_get_device_error", "pa_version"]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(status, "unknown"), status))
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError("libpagedattn.so is not built (%s); run paged_kv_cache_230_gb300.build.build()" % path)
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.pa_reshape_and_cache.argtypes = [P, P, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, f32, P]
+    lib.pa_decode.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
+    lib.pa_decode_split_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
+    lib.pa_decode_split.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
+                                    i32, i32, P, ctypes.c_size_t, P]
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_set_check_mode.argtypes = [ctypes.c_int]
+    lib.pa_get_device_error.argtypes = []
+    lib.pa_version.argtypes = []
+    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_set_check_mode",
+                 "pa_get_device_error", "pa_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return PA_F16
+    if t == torch.bfloat16:
+        return PA_BF16
+    if t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        return PA_FP8_E4M3
+    raise TypeError("unsupported dtype %s" % t)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise PagedAttnError(fn, rc)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, device=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s has dtype %s" % (name, t.dtype))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    NB, Hkv, bs, D = k_cache.shape
+    return CacheDesc(NB, bs, Hkv, D, _dtype_code(k_cache.dtype))
+
+
+def _check_caches(k_cache, v_cache):
+    _need(k_cache, "k_cache", ndim=4)
+    _need(v_cache, "v_cache", ndim=4, device=k_cache.device)
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, kv_scale: float = 1.0) -> None:
+    """Writes key/value rows [T, Hkv, D] into the cache slots named by slot_mapping."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(key, "key", (torch.float16, torch.bfloat16), 3, dev)
+    _need(value, "value", key.dtype, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T = key.shape[0]
+    if value.shape != key.shape or slot_mapping.shape[0] != T:
+        raise ValueError("key/value/slot_mapping shapes disagree")
+    if key.shape[1] != k_cache.shape[1] or key.shape[2] != k_cache.shape[3]:
+        raise ValueError("key rows do not match the cache's heads/head_dim")
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _dtype_code(key.dtype), T, _ptr(k_cache),
+                                      _ptr(v_cache), ctypes.byref(desc), _ptr(slot_mapping), float(kv_scale),
+                                      _stream(dev))
+    _check("pa_reshape_and_cache", rc)
+
+
+def _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens):
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", (torch.float16, torch.bfloat16), 3, dev)
+    _need(out, "out", q.dtype, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S = q.shape[0]
+    if out.shape != q.shape or block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("q/out/block_tables/context_lens shapes disagree")
+    if q.shape[2] != k_cache.shape[3]:
+        raise ValueError("head_dim of q and cache differ")
+    return dev
+
+
+def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float = 1.0) -> None:
+    """Paged decode attention, one CTA per (sequence, kv head); writes out [S, Hq, D]."""
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_decode(_ptr(out), _ptr(q), _dtype_code(q.dtype), q.shape[0], q.shape[1], _ptr(k_cache),
+                           _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1],
+                           _ptr(context_lens), float(scale), float(kv_scale), _stream(dev))
+    _check("pa_decode", rc)
+
+
+def decode_split_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,
+                                partition_size: int) -> int:
+    return int(lib.pa_decode_split_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                                  partition_size))
+
+
+def decode_split(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float,
+                 max_context_len: int, partition_size: int = 512,
+                 workspace: Optional[torch.Tensor] = None) -> None:
+    """Split-context decode: per-partition partials merged by log-sum-exp.
+    ``workspace`` (uint8, at least decode_split_workspace_size bytes) is
+    allocated with torch when not given."""
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
+    need = decode_split_workspace_size(q.shape[0], q.shape[1], q.shape[2], max_context_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", device=dev)
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_decode_split(_ptr(out), _ptr(q), _dtype_code(q.dtype), q.shape[0], q.shape[1],
+                                 _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(context_lens), float(scale), float(kv_scale),
+                                 int(max_context_len), int(partition_size), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(dev))
+    _check("pa_decode_split", rc)
+
+
+def set_check_mode(enable: bool) -> bool:
+    return bool(lib.pa_set_check_mode(1 if enable else 0))
+
+
+def get_device_error() -> int:
+    rc = int(lib.pa_get_device_error())
+    if rc < 0:
+        raise PagedAttnError("pa_get_device_error", rc)
+    return rc
+
+
+def status_string(status: int) -> str:
+    return lib.pa_status_string(status).decode()
