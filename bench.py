@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
     return ap.parse_args()
 
 
@@ -416,6 +417,10 @@ def main():
         return
     seed = args.config + 1000 * rank  # replicas draw independent batches
     wl = W.make_config(args.config, seed=seed)
+    if args.seqs and args.seqs < wl.S:
+        name = "%s_first%d" % (wl.name, args.seqs)
+        wl = W.subset(wl, np.arange(args.seqs))
+        wl.name = name
     if args.impl == "reference":
         run_reference(args, wl, world, rank, pg)
     else:
