@@ -150,6 +150,29 @@ PA_API int pa_decode_split(void *out, const void *q, int32_t q_dtype, int32_t nu
                     int32_t max_context_len, int32_t partition_size, void *workspace,
                     size_t workspace_bytes, pa_stream_t stream);
 
+/*
+ * pa_decode_split_noalloc: pa_decode_split without a workspace argument, for
+ * callers that cannot allocate device memory when they call (for example a
+ * serving process whose KV-cache pool already holds nearly all of HBM, or a
+ * host framework that owns every device allocation of its plug-ins).  The
+ * pages describe no such call; it exists only for those callers.
+ * The partial results go to a 32 MiB scratch array compiled into the library
+ * (held on every device that loads it until the process exits).  Returns
+ * PA_ERR_WORKSPACE when pa_decode_split_workspace_size(num_seqs, num_q_heads,
+ * head_dim, max_context_len, partition_size) exceeds 32 MiB; otherwise the
+ * same arguments, results and errors as pa_decode_split.  The first call on a
+ * device looks up the scratch address (cudaGetSymbolAddress) and should come
+ * before any stream capture.  All calls on a device share the scratch, so
+ * calls that can overlap on the GPU (unordered streams) race; calls ordered
+ * on one stream are safe.  Allocates nothing.
+ */
+PA_API int pa_decode_split_noalloc(void *out, const void *q, int32_t q_dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                   const pa_cache_desc *cache, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t *context_lens, float scale,
+                                   float kv_scale, int32_t max_context_len, int32_t partition_size,
+                                   pa_stream_t stream);
+
 /* Static description of a status code. */
 PA_API const char *pa_status_string(int status);
 

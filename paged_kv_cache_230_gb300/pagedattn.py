@@ -30,7 +30,8 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: 
           -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_split_workspace_size", "pa_decode_split",
-           "pa_status_string", "pa_set_check_mode", "pa_get_device_error", "pa_version"]
+           "pa_decode_split_noalloc", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
+           "pa_version"]
 
 
 class PagedAttnError(RuntimeError):
@@ -56,12 +57,15 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
     lib.pa_decode_split.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
                                     i32, i32, P, ctypes.c_size_t, P]
+    lib.pa_decode_split_noalloc.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32,
+                                            f32, i32, i32, P]
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_set_check_mode.argtypes = [ctypes.c_int]
     lib.pa_get_device_error.argtypes = []
     lib.pa_version.argtypes = []
-    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_set_check_mode",
+    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_noalloc",
+                 "pa_set_check_mode",
                  "pa_get_device_error", "pa_version"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
