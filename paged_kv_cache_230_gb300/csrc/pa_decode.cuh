@@ -171,8 +171,96 @@ __device__ __forceinline__ void load_piece(const uint8_t* src, float* f) {
   }
 }
 
+// Dispatch order.  CTAs start roughly in blockIdx order, so handing the
+// longest contexts to the first CTAs gives longest-first list scheduling and
+// removes the tail where a long sequence starts late.  Lengths are ranked by
+// a 128-bucket key (4 buckets per power of two), descending, ties by sequence
+// index; CTA rank r processes the sequence of rank r.  Computed by every CTA
+// from context_lens with one histogram and one block-wide scan (no scratch
+// memory), identically in all CTAs, so the mapping is a permutation.
+constexpr int kOrderBuckets = 128;
+
+__device__ __forceinline__ int length_bucket_desc(int L) {
+  if (L <= 0) return kOrderBuckets - 1;
+  const int msb = 31 - __clz(L);
+  const int frac = msb >= 2 ? (L >> (msb - 2)) & 3 : (L << (2 - msb)) & 3;
+  return kOrderBuckets - 1 - min(msb * 4 + frac, kOrderBuckets - 1);
+}
+
+// All kThreads threads call this; returns the sequence of rank r.
+__device__ __noinline__ static int seq_of_rank(const int32_t* __restrict__ context_lens, int S, int r) {
+  __shared__ int hist[kOrderBuckets];
+  __shared__ int warp_tot[kThreads / 32];
+  __shared__ int sel[3];  // bucket, index inside the bucket, chosen sequence
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kOrderBuckets; i += kThreads) hist[i] = 0;
+  if (tid == 0) sel[2] = min(r, S - 1);
+  __syncthreads();
+  const int per = (S + kThreads - 1) / kThreads;  // contiguous chunk of sequences per thread
+  const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+  for (int i = 0; i < per; ++i) {  // same trip count in every lane: one atomic per distinct bucket
+    const int s = s0 + i;
+    const int b = s < s1 ? length_bucket_desc(__ldg(context_lens + s)) : -1;
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, b);
+    if (b >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[b], __popc(same));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the histogram (4 buckets per lane), then locate r
+    int c[4], run = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      c[k] = hist[lane * 4 + k];
+      run += c[k];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int base = incl - run;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (r >= base && r < base + c[k]) {
+        sel[0] = lane * 4 + k;
+        sel[1] = r - base;
+      }
+      base += c[k];
+    }
+  }
+  __syncthreads();
+  const int bucket = sel[0], want = sel[1];
+  int mine = 0;
+  for (int s = s0; s < s1; ++s) mine += length_bucket_desc(__ldg(context_lens + s)) == bucket;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int before = incl - mine;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  if (want >= before && want < before + mine) {
+    int k = want - before;
+    for (int s = s0; s < s1; ++s) {
+      if (length_bucket_desc(__ldg(context_lens + s)) == bucket) {
+        if (k == 0) {
+          sel[2] = s;
+          break;
+        }
+        --k;
+      }
+    }
+  }
+  __syncthreads();
+  return min(max(sel[2], 0), S - 1);
+}
+
 template <int KV, int D, bool USE_MMA, int NG>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   using Gm = Geom<KV, D>;
@@ -197,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int part = bid % p.Pmax;
   bid /= p.Pmax;
   const int h = bid % p.Hkv;
-  const int s = bid / p.Hkv;
+  const int s = p.S > 1 ? seq_of_rank(p.context_lens, p.S, bid / p.Hkv) : 0;
   const bool split = p.partition_size > 0;
   int lmax = p.maxB * p.bs;
   if (split) lmax = min(lmax, p.Pmax * p.partition_size);
@@ -301,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   named_bar_sync(1, NCW * 32);
   if constexpr (KV == kE4M3 && USE_MMA) {
-    qmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    qmax = red[0];
+#pragma unroll
+    for (int w = 1; w < NCW; ++w) qmax = fmaxf(qmax, red[w]);
     int e = 0;
     if (qmax > 0.f) {
       int ex;

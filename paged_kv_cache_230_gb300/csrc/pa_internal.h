@@ -8,10 +8,21 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;                 // warps that compute
+// Pipeline shape (compile-time; the defaults are the measured best on GB300).
+#ifndef PA_CONSUMER_WARPS
+#define PA_CONSUMER_WARPS 4
+#endif
+#ifndef PA_RING_KB
+#define PA_RING_KB 96
+#endif
+#ifndef PA_MIN_CTAS_PER_SM
+#define PA_MIN_CTAS_PER_SM 2
+#endif
+constexpr int kConsumerWarps = PA_CONSUMER_WARPS;    // warps that compute
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kTileTokens = 16 * kConsumerWarps;  // tokens per pipeline stage
-constexpr int kRingBytes = 96 * 1024;             // target bytes of the K/V stage ring
+constexpr int kTileTokens = 16 * kConsumerWarps;     // tokens per pipeline stage
+constexpr int kRingBytes = PA_RING_KB * 1024;        // target bytes of the K/V stage ring
+constexpr int kMinCtasPerSm = PA_MIN_CTAS_PER_SM;
 constexpr int kMaxGroup = 16;                     // largest query group G
 
 enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
