@@ -175,6 +175,7 @@ pa::DecodeParams make_params(const DecodeArgs& a, int* err) {
   p.q_dtype = a.q_dtype;
   p.partition_size = 0;
   p.Pmax = 1;
+  p.parts_per_cta = 1;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.kv_scale = a.cache->kv_dtype == PA_FP8_E4M3 ? a.kv_scale : 1.0f;
   return p;
@@ -187,6 +188,26 @@ cudaError_t launch_decode(const pa::DecodeParams& p, const CUtensorMap& tk, cons
     case PA_BF16: return pa::launch_decode_bf16(p, tk, tv, head_dim, st);
     default: return pa::launch_decode_fp8(p, tk, tv, head_dim, st);
   }
+}
+
+// Consecutive partitions one split CTA streams: enough that the grid holds
+// about four CTAs per resident slot when every sequence has Pmax partitions,
+// so launch and pipeline ramp costs are paid per run, not per partition.
+int parts_per_cta(int S, int Hkv, int Pmax) {
+  static int sms[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    sms[dev] = n;
+  }
+  const int64_t target = int64_t(4) * sms[dev] * pa::kMinCtasPerSm;
+  const int64_t total = int64_t(S) * Hkv * Pmax;
+  int64_t ppc = (total + target - 1) / target;
+  if (ppc < 1) ppc = 1;
+  if (ppc > Pmax) ppc = Pmax;
+  return static_cast<int>(ppc);
 }
 
 int64_t split_partitions(int32_t max_context_len, int32_t partition_size) {
@@ -281,6 +302,7 @@ int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
   pa::DecodeParams p = make_params(a, err);
   p.partition_size = partition_size;
   p.Pmax = static_cast<int>(np);
+  p.parts_per_cta = parts_per_cta(num_seqs, cache->num_kv_heads, p.Pmax);
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * np;
   p.ws_ml = static_cast<float*>(workspace);
   p.ws_o = p.ws_ml + rows * 2;

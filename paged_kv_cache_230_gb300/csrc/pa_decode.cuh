@@ -74,7 +74,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 
 template <int NG, int D>
 __host__ __device__ constexpr int decode_smem_bytes_for(int ring, int nst) {
-  return 1024 + ring + NG * D * 4 + 2 * nst * 8 + 64;
+  return 1024 + ring + NG * D * 4 + 2 * nst * 8 + kConsumerWarps * NG * 2 * 4;
 }
 
 template <int KV, int D, int NG>
@@ -259,49 +259,116 @@ __device__ __noinline__ static int seq_of_rank(const int32_t* __restrict__ conte
   return min(max(sel[2], 0), S - 1);
 }
 
+// Combination of the consumer warps' partial states for one segment (the
+// whole token range, or one partition in the split variant).  Every warp has
+// written its (m, l) per head to ml[w][g]; the warps then add their rescaled
+// outputs 2^(m_w - M) o_w into `area` ([NG][D] floats) one after the other in
+// warp order (`add_mine` is called by warp w on its turn), and finally all
+// consumer threads write the normalised output or the unnormalised partial.
+template <int D, int NG, class AddMine>
+__device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, int ctid, float* area,
+                                                 const float* ml, int64_t qrow0, bool single, int part,
+                                                 float vscale, AddMine add_mine) {
+  constexpr int NCW = kConsumerWarps;
+  named_bar_sync(1, NCW * 32);  // every warp's (m, l) is visible
+#pragma unroll 1
+  for (int w = 0; w < NCW; ++w) {
+    if (cw == w) add_mine(w == 0);
+    named_bar_sync(1, NCW * 32);
+  }
+  for (int idx = ctid; idx < p.G * D; idx += NCW * 32) {
+    const int g = idx / D, d = idx % D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * NG + g) * 2]);
+    float lsum = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) lsum += ml[(w * NG + g) * 2 + 1] * ex2(ml[(w * NG + g) * 2] - M);
+    }
+    const float acc = area[g * D + d] * vscale;
+    const int64_t row = qrow0 + g;
+    if (single) {
+      store_out(p.out, row * D + d, p.q_dtype, lsum > 0.f ? acc / lsum : 0.f);
+    } else {
+      const int64_t slot = row * p.Pmax + part;
+      p.ws_o[slot * D + d] = acc;
+      if (d == 0) {
+        p.ws_ml[2 * slot] = M;
+        p.ws_ml[2 * slot + 1] = lsum;
+      }
+    }
+  }
+  named_bar_sync(1, NCW * 32);  // area and ml may be reused
+}
+
+// Scale factor of warp w's state for head g: 2^(m_w - M), M = max over warps.
+template <int NG>
+__device__ __forceinline__ float warp_factor(const float* ml, int w, int g) {
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int v = 0; v < kConsumerWarps; ++v) M = fmaxf(M, ml[(v * NG + g) * 2]);
+  return M == -CUDART_INF_F ? 0.f : ex2(ml[(w * NG + g) * 2] - M);
+}
+
+// CTAs per SM the register budget is sized for: the widest variants (16
+// heads per MMA, or 3 heads on the shuffle path with 128 channels) hold too
+// many accumulators for three.
+template <int D, bool USE_MMA, int NG>
+constexpr int decode_min_ctas() {
+  return ((USE_MMA && NG > 8) || (!USE_MMA && NG > 1 && D > 64)) ? (kMinCtasPerSm < 2 ? kMinCtasPerSm : 2)
+                                                                 : kMinCtasPerSm;
+}
+
 template <int KV, int D, bool USE_MMA, int NG>
-__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
+__global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   using Gm = Geom<KV, D>;
   constexpr int NST = Gm::NST;
   constexpr int NCW = kConsumerWarps;
   constexpr int TILE = kTileTokens;
-  static_assert(NCW * NG * D * 4 + 2 * NCW * NG * 4 <= Gm::RING, "merge area must fit in the ring");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
   const uint32_t ring_u32 = smem_u32(smem);
-  float* qbuf = reinterpret_cast<float*>(smem + Gm::RING);  // [NG][D]
+  // q staging at start-up, then the epilogue's output area: [NG][D] floats
+  float* qbuf = reinterpret_cast<float*>(smem + Gm::RING);
+  float* area = qbuf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::RING + NG * D * 4);
-  float* red = reinterpret_cast<float*>(bars + 2 * NST);     // 16 floats
+  float* ml = reinterpret_cast<float*>(bars + 2 * NST);  // [NCW][NG][2]
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + NST * 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- which (sequence, kv head, partition) ----
+  // ---- which (sequence, kv head, run of partitions) ----
+  // Split variant: CTA c of a (sequence, kv head) owns partitions
+  // [c * ppc, (c + 1) * ppc) and streams them back to back.
+  const bool split = p.partition_size > 0;
+  const int nchunk = split ? (p.Pmax + p.parts_per_cta - 1) / p.parts_per_cta : 1;
   int bid = blockIdx.x;
-  const int part = bid % p.Pmax;
-  bid /= p.Pmax;
+  const int chunk = bid % nchunk;
+  bid /= nchunk;
   const int h = bid % p.Hkv;
   const int s = p.S > 1 ? seq_of_rank(p.context_lens, p.S, bid / p.Hkv) : 0;
-  const bool split = p.partition_size > 0;
   int lmax = p.maxB * p.bs;
   if (split) lmax = min(lmax, p.Pmax * p.partition_size);
   int L = p.context_lens[s];
   if (L < 0 || L > lmax) {
-    if (tid == 0 && part == 0 && h == 0) atomicOr(p.err, kErrContextLen);
+    if (tid == 0 && chunk == 0 && h == 0) atomicOr(p.err, kErrContextLen);
     L = min(max(L, 0), lmax);
   }
-  int tok_begin = 0, tok_end = L;
+  int tok_begin = 0, tok_end = L, part_first = 0;
   if (split) {
-    tok_begin = part * p.partition_size;
-    tok_end = min(L, tok_begin + p.partition_size);
-    if (part > 0 && tok_begin >= L) return;  // partition past the end of this context
+    part_first = chunk * p.parts_per_cta;
+    tok_begin = part_first * p.partition_size;
+    tok_end = min(L, (part_first + p.parts_per_cta) * p.partition_size);
+    if (chunk > 0 && tok_begin >= L) return;  // past the end of this context
   }
-  const bool single = !split || L <= p.partition_size;  // this CTA writes the final output
+  const bool single = !split || L <= p.partition_size;  // the final output is written here
   const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TILE - 1) / TILE : 0;
+  const int tiles_per_seg = split ? p.partition_size / TILE : max(ntiles, 1);
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -370,13 +437,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   // ========================= consumer warps =========================
   const int cw = warp;
-  const int ctid = tid;  // 0..127
-  const int qrow0 = s * p.Hq + h * p.G;
+  const int ctid = tid;  // 0..NCW*32-1
+  const int64_t qrow0 = static_cast<int64_t>(s) * p.Hq + h * p.G;
   float qmax = 0.f;
   for (int idx = ctid; idx < NG * D; idx += NCW * 32) {
     const int g = idx / D, d = idx % D;
     float v = 0.f;
-    if (g < p.G) v = load_q(p.q, static_cast<int64_t>(qrow0 + g) * D + d, p.q_dtype);
+    if (g < p.G) v = load_q(p.q, (qrow0 + g) * D + d, p.q_dtype);
     qbuf[idx] = v;
     qmax = fmaxf(qmax, fabsf(v));
   }
@@ -385,13 +452,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   if constexpr (KV == kE4M3 && USE_MMA) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, o));
-    if (lane == 0) red[cw] = qmax;
+    if (lane == 0) ml[cw] = qmax;
   }
   named_bar_sync(1, NCW * 32);
   if constexpr (KV == kE4M3 && USE_MMA) {
-    qmax = red[0];
+    qmax = ml[0];
 #pragma unroll
-    for (int w = 1; w < NCW; ++w) qmax = fmaxf(qmax, red[w]);
+    for (int w = 1; w < NCW; ++w) qmax = fmaxf(qmax, ml[w]);
     int e = 0;
     if (qmax > 0.f) {
       int ex;
@@ -401,8 +468,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     qmul = ldexpf(1.f, e);
     qk_mult = ldexpf(qk_mult, -e);
   }
-
+  const float vscale = (KV == kE4M3) ? p.kv_scale : 1.f;
   const int qr = lane >> 2, qc = lane & 3;
+  const int row0 = cw * 16;
 
   if constexpr (USE_MMA) {
     constexpr int NT = NG / 8;   // head tiles of 8
@@ -425,15 +493,59 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         }
       }
     }
+    named_bar_sync(1, NCW * 32);  // qbuf is free: it becomes the epilogue area
     float m_run[NT][2], l_run[NT][2], oacc[KS][NT][4];
+    auto reset = [&]() {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
-      l_run[nt][0] = l_run[nt][1] = 0.f;
+      for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
-    }
-    const int row0 = cw * 16;
+        for (int mt = 0; mt < KS; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
+      }
+    };
+    // (m, l) of this warp to ml[], then its rescaled output into `area` on its turn
+    auto epilogue = [&](int part) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float l = l_run[nt][c2];
+          l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
+          l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+          l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+          if (qr == 0) {
+            const int g = nt * 8 + 2 * qc + c2;
+            ml[(cw * NG + g) * 2] = m_run[nt][c2];
+            ml[(cw * NG + g) * 2 + 1] = l;
+          }
+        }
+      }
+      segment_epilogue<D, NG>(p, cw, ctid, area, ml, qrow0, single, part, vscale, [&](bool first) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float f0 = warp_factor<NG>(ml, cw, nt * 8 + 2 * qc);
+          const float f1 = warp_factor<NG>(ml, cw, nt * 8 + 2 * qc + 1);
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int g = nt * 8 + 2 * qc + (e & 1);
+              int d;
+              if constexpr (KV == kE4M3) {
+                d = 16 * mt + 4 * (qr >> 1) + (qr & 1) + (e >= 2 ? 2 : 0);
+              } else {
+                d = 16 * mt + qr + (e >= 2 ? 8 : 0);
+              }
+              const float v = oacc[mt][nt][e] * ((e & 1) ? f1 : f0);
+              area[g * D + d] = first ? v : area[g * D + d] + v;
+            }
+          }
+        }
+      });
+    };
+    reset();
+    int seg_t = 0;  // tiles done in the current segment
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % NST;
       if (!mbar_wait(full0 + 8 * stage, (t / NST) & 1)) {
@@ -552,51 +664,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * stage);
-    }
-
-    // ---- merge the four warps' partial states ----
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        float l = l_run[nt][c2];
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
-        l_run[nt][c2] = l;
+      if (++seg_t == tiles_per_seg && t + 1 < ntiles) {  // a partition ends inside this CTA's run
+        epilogue(part_first + t / tiles_per_seg);
+        reset();
+        seg_t = 0;
       }
     }
-    named_bar_sync(1, NCW * 32);  // every consumer is done reading the ring
-    float* os = reinterpret_cast<float*>(smem);  // [NCW][NG][D]
-    float* msb = os + NCW * NG * D;              // [NCW][NG]
-    float* lsb = msb + NCW * NG;
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int g = nt * 8 + 2 * qc + (e & 1);
-          int d;
-          if constexpr (KV == kE4M3) {
-            d = 16 * mt + 4 * (qr >> 1) + (qr & 1) + (e >= 2 ? 2 : 0);
-          } else {
-            d = 16 * mt + qr + (e >= 2 ? 8 : 0);
-          }
-          os[(cw * NG + g) * D + d] = oacc[mt][nt][e];
-        }
-      }
-    }
-    if (qr == 0) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int g = nt * 8 + 2 * qc + c2;
-          msb[cw * NG + g] = m_run[nt][c2];
-          lsb[cw * NG + g] = l_run[nt][c2];
-        }
-    }
+    epilogue(part_first + (ntiles > 0 ? (ntiles - 1) / tiles_per_seg : 0));
   } else {
     // ================= warp-shuffle path (G <= 3) =================
     constexpr int EPL = D / 8;              // elements per lane per row
@@ -610,15 +684,63 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       for (int sg = 0; sg < Gm::NSEG; ++sg)
 #pragma unroll
         for (int e = 0; e < EPS; ++e) qv[g][sg * EPS + e] = qbuf[g * D + sg * Gm::BOXE + sub * EPS + e];
+    named_bar_sync(1, NCW * 32);  // qbuf is free: it becomes the epilogue area
     float m_run[NG], l_run[NG], o[NG][EPL];
+    auto reset = [&]() {
 #pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      m_run[g] = -CUDART_INF_F;
-      l_run[g] = 0.f;
+      for (int g = 0; g < NG; ++g) {
+        m_run[g] = -CUDART_INF_F;
+        l_run[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) o[g][e] = 0.f;
-    }
-    const int row0 = cw * 16;
+        for (int e = 0; e < EPL; ++e) o[g][e] = 0.f;
+      }
+    };
+    auto epilogue = [&](int part) {
+      // merge the four 8-lane groups (commutative, so every lane gets the same bits)
+#pragma unroll
+      for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const float m_o = __shfl_xor_sync(0xFFFFFFFFu, m_run[g], off);
+          const float l_o = __shfl_xor_sync(0xFFFFFFFFu, l_run[g], off);
+          const float M = fmaxf(m_run[g], m_o);
+          const float M_use = M == -CUDART_INF_F ? 0.f : M;
+          const float a = ex2(m_run[g] - M_use), b = ex2(m_o - M_use);
+          l_run[g] = l_run[g] * a + l_o * b;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            const float o_o = __shfl_xor_sync(0xFFFFFFFFu, o[g][e], off);
+            o[g][e] = o[g][e] * a + o_o * b;
+          }
+          m_run[g] = M;
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          ml[(cw * NG + g) * 2] = m_run[g];
+          ml[(cw * NG + g) * 2 + 1] = l_run[g];
+        }
+      }
+      segment_epilogue<D, NG>(p, cw, ctid, area, ml, qrow0, single, part, vscale, [&](bool first) {
+        if (grp == 0) {
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float f = warp_factor<NG>(ml, cw, g);
+#pragma unroll
+            for (int sg = 0; sg < Gm::NSEG; ++sg)
+#pragma unroll
+              for (int e = 0; e < EPS; ++e) {
+                const int d = sg * Gm::BOXE + sub * EPS + e;
+                const float v = o[g][sg * EPS + e] * f;
+                area[g * D + d] = first ? v : area[g * D + d] + v;
+              }
+          }
+        }
+      });
+    };
+    reset();
+    int seg_t = 0;
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % NST;
       if (!mbar_wait(full0 + 8 * stage, (t / NST) & 1)) {
@@ -682,79 +804,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * stage);
-    }
-    // merge the four 8-lane groups (commutative, so every lane gets the same bits)
-#pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        const float m_o = __shfl_xor_sync(0xFFFFFFFFu, m_run[g], off);
-        const float l_o = __shfl_xor_sync(0xFFFFFFFFu, l_run[g], off);
-        const float M = fmaxf(m_run[g], m_o);
-        const float M_use = M == -CUDART_INF_F ? 0.f : M;
-        const float a = ex2(m_run[g] - M_use), b = ex2(m_o - M_use);
-        l_run[g] = l_run[g] * a + l_o * b;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          const float o_o = __shfl_xor_sync(0xFFFFFFFFu, o[g][e], off);
-          o[g][e] = o[g][e] * a + o_o * b;
-        }
-        m_run[g] = M;
+      if (++seg_t == tiles_per_seg && t + 1 < ntiles) {
+        epilogue(part_first + t / tiles_per_seg);
+        reset();
+        seg_t = 0;
       }
     }
-    named_bar_sync(1, NCW * 32);
-    float* os = reinterpret_cast<float*>(smem);
-    float* msb = os + NCW * NG * D;
-    float* lsb = msb + NCW * NG;
-    if (grp == 0) {
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-#pragma unroll
-        for (int sg = 0; sg < Gm::NSEG; ++sg)
-#pragma unroll
-          for (int e = 0; e < EPS; ++e) os[(cw * NG + g) * D + sg * Gm::BOXE + sub * EPS + e] = o[g][sg * EPS + e];
-        if (sub == 0) {
-          msb[cw * NG + g] = m_run[g];
-          lsb[cw * NG + g] = l_run[g];
-        }
-      }
-    }
-  }
-
-  // ---- final combination of the four warps, in warp order ----
-  named_bar_sync(1, NCW * 32);
-  {
-    const float* os = reinterpret_cast<const float*>(smem);
-    const float* msb = os + NCW * NG * D;
-    const float* lsb = msb + NCW * NG;
-    const float vscale = (KV == kE4M3) ? p.kv_scale : 1.f;
-    for (int idx = ctid; idx < p.G * D; idx += NCW * 32) {
-      const int g = idx / D, d = idx % D;
-      float M = -CUDART_INF_F;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) M = fmaxf(M, msb[w * NG + g]);
-      float lsum = 0.f, acc = 0.f;
-      if (M != -CUDART_INF_F) {
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-          const float sc = ex2(msb[w * NG + g] - M);
-          lsum += lsb[w * NG + g] * sc;
-          acc += os[(w * NG + g) * D + d] * sc;
-        }
-      }
-      acc *= vscale;
-      const int64_t row = qrow0 + g;
-      if (single) {
-        store_out(p.out, row * D + d, p.q_dtype, lsum > 0.f ? acc / lsum : 0.f);
-      } else {
-        const int64_t slot = row * p.Pmax + part;
-        p.ws_o[slot * D + d] = acc;
-        if (d == 0) {
-          p.ws_ml[2 * slot] = M;
-          p.ws_ml[2 * slot + 1] = lsum;
-        }
-      }
-    }
+    epilogue(part_first + (ntiles > 0 ? (ntiles - 1) / tiles_per_seg : 0));
   }
 }
 
@@ -788,7 +844,8 @@ cudaError_t launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUte
   auto kern = decode_kernel<KV, D, USE_MMA, NG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(p.S) * p.Hkv * p.Pmax;
+  const int nchunk = p.partition_size > 0 ? (p.Pmax + p.parts_per_cta - 1) / p.parts_per_cta : 1;
+  const long long grid = static_cast<long long>(p.S) * p.Hkv * nchunk;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmK, tmV, p);
   return cudaGetLastError();
 }

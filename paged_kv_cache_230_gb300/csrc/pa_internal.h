@@ -13,10 +13,10 @@ namespace pa {
 #define PA_CONSUMER_WARPS 4
 #endif
 #ifndef PA_RING_KB
-#define PA_RING_KB 96
+#define PA_RING_KB 64
 #endif
 #ifndef PA_MIN_CTAS_PER_SM
-#define PA_MIN_CTAS_PER_SM 2
+#define PA_MIN_CTAS_PER_SM 3
 #endif
 constexpr int kConsumerWarps = PA_CONSUMER_WARPS;    // warps that compute
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
@@ -39,7 +39,8 @@ struct DecodeParams {
   int S, Hq, Hkv, G, bs, maxB;
   int q_dtype;
   int partition_size;         // tokens per partition; 0 = whole context per CTA
-  int Pmax;                   // partitions per sequence in the grid (1 without split)
+  int Pmax;                   // partitions per sequence (1 without split)
+  int parts_per_cta;          // split: consecutive partitions streamed by one CTA
   float scale_log2;           // scale * log2(e)
   float kv_scale;             // FP8 dequantisation scale (1 for 16-bit caches)
 };
