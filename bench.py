@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
+    ap.add_argument("--ref-budget", type=float, default=0.0,
+                    help="reference arm: seconds of oracle work per step (default min(20, 120 / steps))")
     return ap.parse_args()
 
 
@@ -239,11 +241,11 @@ def run_reference(args, wl, world, rank, pg):
     if rank != 0:
         return
     steps = max(1, args.steps)
-    per_step = max(2.0, 60.0 / steps)
+    per_step = args.ref_budget if args.ref_budget > 0 else min(20.0, 120.0 / steps)
     secs, byts, nseq = 0.0, 0, 0
     threads = 1
     for _ in range(max(0, min(args.warmup, 1))):
-        oracle_sample_time(wl, budget_s=0.5)
+        oracle_sample_time(wl, budget_s=min(0.5, per_step))
     for _ in range(steps):
         t, b, n, threads = oracle_sample_time(wl, budget_s=per_step)
         secs += t
