@@ -6,7 +6,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/pagedattn.h"
+#include "pagedattn.h"
 #include "pa_internal.h"
 
 namespace {
@@ -191,8 +191,12 @@ cudaError_t launch_decode(const pa::DecodeParams& p, const CUtensorMap& tk, cons
 }
 
 // Consecutive partitions one split CTA streams: enough that the grid holds
-// about four CTAs per resident slot when every sequence has Pmax partitions,
-// so launch and pipeline ramp costs are paid per run, not per partition.
+// about PA_SPLIT_CTAS_PER_SLOT CTAs per resident slot when every sequence has
+// Pmax partitions, so launch and pipeline ramp costs are paid per run, not
+// per partition.
+#ifndef PA_SPLIT_CTAS_PER_SLOT
+#define PA_SPLIT_CTAS_PER_SLOT 8
+#endif
 int parts_per_cta(int S, int Hkv, int Pmax) {
   static int sms[kMaxDevices] = {0};
   int dev = 0;
@@ -202,7 +206,7 @@ int parts_per_cta(int S, int Hkv, int Pmax) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
     sms[dev] = n;
   }
-  const int64_t target = int64_t(4) * sms[dev] * pa::kMinCtasPerSm;
+  const int64_t target = int64_t(PA_SPLIT_CTAS_PER_SLOT) * sms[dev] * pa::kMinCtasPerSm;
   const int64_t total = int64_t(S) * Hkv * Pmax;
   int64_t ppc = (total + target - 1) / target;
   if (ppc < 1) ppc = 1;

@@ -74,7 +74,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 
 template <int NG, int D>
 __host__ __device__ constexpr int decode_smem_bytes_for(int ring, int nst) {
-  return 1024 + ring + NG * D * 4 + 2 * nst * 8 + kConsumerWarps * NG * 2 * 4;
+  return 1024 + ring + 2 * NG * D * 4 + 2 * nst * 8 + kConsumerWarps * NG * 2 * 4 + 2 * NG * 2 * 4;
 }
 
 template <int KV, int D, int NG>
@@ -260,15 +260,30 @@ __device__ __noinline__ static int seq_of_rank(const int32_t* __restrict__ conte
 }
 
 // Combination of the consumer warps' partial states for one segment (the
-// whole token range, or one partition in the split variant).  Every warp has
-// written its (m, l) per head to ml[w][g]; the warps then add their rescaled
-// outputs 2^(m_w - M) o_w into `area` ([NG][D] floats) one after the other in
-// warp order (`add_mine` is called by warp w on its turn), and finally all
-// consumer threads write the normalised output or the unnormalised partial.
+// whole token range, or one 512-token partition in the split variant).
+// Every warp has written its (m, l) per head to ml[w][g]; the warps then add
+// their rescaled outputs 2^(m_w - M) o_w into `area` ([NG][D] floats) one
+// after the other in warp order (`add_mine` is called by warp w on its turn).
+// Then, per output element:
+//  - one-pass decode, or a context whose partitions all belong to this CTA:
+//    the partition partials are folded into the run accumulator (`carea`,
+//    `cml`) by log-sum-exp, and the last segment writes o / l;
+//  - otherwise the run's log-sum-exp of its partitions is written to the
+//    workspace as one partial (slot = this CTA's run), merged later by
+//    lse_merge_kernel.  The two levels together are the log-sum-exp merge of
+//    all 512-token partitions, in a fixed order.
+struct SegInfo {
+  int seg;        // segment index inside this CTA's run
+  bool last;      // last segment of the run
+  bool split;     // split variant
+  bool final_out; // this CTA writes the normalised output
+  int chunk;      // the run's index (workspace slot)
+};
+
 template <int D, int NG, class AddMine>
 __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, int ctid, float* area,
-                                                 const float* ml, int64_t qrow0, bool single, int part,
-                                                 float vscale, AddMine add_mine) {
+                                                 float* carea, float* cml, const float* ml, int64_t qrow0,
+                                                 const SegInfo& si, float vscale, AddMine add_mine) {
   constexpr int NCW = kConsumerWarps;
   named_bar_sync(1, NCW * 32);  // every warp's (m, l) is visible
 #pragma unroll 1
@@ -276,6 +291,8 @@ __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, 
     if (cw == w) add_mine(w == 0);
     named_bar_sync(1, NCW * 32);
   }
+  const float* cml_in = cml + ((si.seg + 1) & 1) * NG * 2;  // run state before this segment
+  float* cml_out = cml + (si.seg & 1) * NG * 2;
   for (int idx = ctid; idx < p.G * D; idx += NCW * 32) {
     const int g = idx / D, d = idx % D;
     float M = -CUDART_INF_F;
@@ -286,12 +303,32 @@ __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, 
 #pragma unroll
       for (int w = 0; w < NCW; ++w) lsum += ml[(w * NG + g) * 2 + 1] * ex2(ml[(w * NG + g) * 2] - M);
     }
-    const float acc = area[g * D + d] * vscale;
+    float acc = area[g * D + d] * vscale;
     const int64_t row = qrow0 + g;
-    if (single) {
+    if (si.split) {
+      // fold this partition into the run: log-sum-exp of (run so far, partition)
+      if (si.seg > 0) {
+        const float Mc = cml_in[2 * g], Lc = cml_in[2 * g + 1];
+        const float M2 = fmaxf(Mc, M);
+        const float fa = Mc == -CUDART_INF_F ? 0.f : ex2(Mc - M2);
+        const float fb = M == -CUDART_INF_F ? 0.f : ex2(M - M2);
+        acc = carea[g * D + d] * fa + acc * fb;
+        lsum = Lc * fa + lsum * fb;
+        M = M2;
+      }
+      if (!si.last) {
+        carea[g * D + d] = acc;
+        if (d == 0) {
+          cml_out[2 * g] = M;
+          cml_out[2 * g + 1] = lsum;
+        }
+        continue;
+      }
+    }
+    if (si.final_out) {
       store_out(p.out, row * D + d, p.q_dtype, lsum > 0.f ? acc / lsum : 0.f);
     } else {
-      const int64_t slot = row * p.Pmax + part;
+      const int64_t slot = row * p.Pmax + si.chunk;
       p.ws_o[slot * D + d] = acc;
       if (d == 0) {
         p.ws_ml[2 * slot] = M;
@@ -299,7 +336,7 @@ __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, 
       }
     }
   }
-  named_bar_sync(1, NCW * 32);  // area and ml may be reused
+  named_bar_sync(1, NCW * 32);  // area, carea and ml may be reused
 }
 
 // Scale factor of warp w's state for head g: 2^(m_w - M), M = max over warps.
@@ -338,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
   float* area = qbuf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::RING + NG * D * 4);
   float* ml = reinterpret_cast<float*>(bars + 2 * NST);  // [NCW][NG][2]
+  float* cml = ml + NCW * NG * 2;                         // [2][NG][2] run (m, l), double-buffered
+  float* carea = reinterpret_cast<float*>(smem + Gm::RING + NG * D * 4 + 2 * NST * 8 + (NCW + 2) * NG * 2 * 4);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + NST * 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -366,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     tok_end = min(L, (part_first + p.parts_per_cta) * p.partition_size);
     if (chunk > 0 && tok_begin >= L) return;  // past the end of this context
   }
-  const bool single = !split || L <= p.partition_size;  // the final output is written here
+  // this CTA holds every partition of the context: it writes the final output
+  const bool final_out = !split || L <= p.parts_per_cta * p.partition_size;
   const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TILE - 1) / TILE : 0;
   const int tiles_per_seg = split ? p.partition_size / TILE : max(ntiles, 1);
 
@@ -505,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
       }
     };
     // (m, l) of this warp to ml[], then its rescaled output into `area` on its turn
-    auto epilogue = [&](int part) {
+    auto epilogue = [&](int seg, bool last) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -521,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           }
         }
       }
-      segment_epilogue<D, NG>(p, cw, ctid, area, ml, qrow0, single, part, vscale, [&](bool first) {
+      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, qrow0, SegInfo{seg, last, split, final_out, chunk},
+                              vscale, [&](bool first) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float f0 = warp_factor<NG>(ml, cw, nt * 8 + 2 * qc);
@@ -665,12 +706,12 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * stage);
       if (++seg_t == tiles_per_seg && t + 1 < ntiles) {  // a partition ends inside this CTA's run
-        epilogue(part_first + t / tiles_per_seg);
+        epilogue(t / tiles_per_seg, false);
         reset();
         seg_t = 0;
       }
     }
-    epilogue(part_first + (ntiles > 0 ? (ntiles - 1) / tiles_per_seg : 0));
+    epilogue(ntiles > 0 ? (ntiles - 1) / tiles_per_seg : 0, true);
   } else {
     // ================= warp-shuffle path (G <= 3) =================
     constexpr int EPL = D / 8;              // elements per lane per row
@@ -695,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
         for (int e = 0; e < EPL; ++e) o[g][e] = 0.f;
       }
     };
-    auto epilogue = [&](int part) {
+    auto epilogue = [&](int seg, bool last) {
       // merge the four 8-lane groups (commutative, so every lane gets the same bits)
 #pragma unroll
       for (int off = 8; off <= 16; off <<= 1) {
@@ -722,7 +763,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           ml[(cw * NG + g) * 2 + 1] = l_run[g];
         }
       }
-      segment_epilogue<D, NG>(p, cw, ctid, area, ml, qrow0, single, part, vscale, [&](bool first) {
+      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, qrow0, SegInfo{seg, last, split, final_out, chunk},
+                              vscale, [&](bool first) {
         if (grp == 0) {
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
@@ -805,17 +847,17 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * stage);
       if (++seg_t == tiles_per_seg && t + 1 < ntiles) {
-        epilogue(part_first + t / tiles_per_seg);
+        epilogue(t / tiles_per_seg, false);
         reset();
         seg_t = 0;
       }
     }
-    epilogue(part_first + (ntiles > 0 ? (ntiles - 1) / tiles_per_seg : 0));
+    epilogue(ntiles > 0 ? (ntiles - 1) / tiles_per_seg : 0, true);
   }
 }
 
 // Log-sum-exp merge of the split partials of one (sequence, query head) per
-// CTA of 256 threads:  M = max_p m_p,  w_p = 2^(m_p - M),  L = sum_p l_p w_p,
+// CTA of 256 threads (one partial per run of partitions):  M = max_p m_p,  w_p = 2^(m_p - M),  L = sum_p l_p w_p,
 // out = sum_p w_p o_p / L.  The partitions are spread over the threads (the
 // partials are read with independent loads), and every sum is reduced in a
 // fixed order, so the result is deterministic.
@@ -848,8 +890,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodePa
   const int s = row / p.Hq;
   const int lmax = min(p.maxB * p.bs, p.Pmax * p.partition_size);
   const int L = min(max(p.context_lens[s], 0), lmax);
-  const int np = (L + p.partition_size - 1) / p.partition_size;
-  if (np <= 1) return;  // written directly by its only partition
+  const int nparts = (L + p.partition_size - 1) / p.partition_size;
+  const int np = (nparts + p.parts_per_cta - 1) / p.parts_per_cta;  // runs, one partial each
+  if (np <= 1) return;  // written directly by the CTA that held every partition
   const int tid = threadIdx.x;
   const float* ml = p.ws_ml + static_cast<int64_t>(row) * p.Pmax * 2;
   const float* o = p.ws_o + static_cast<int64_t>(row) * p.Pmax * D;

@@ -20,7 +20,7 @@
 // merge reads is written earlier by the same call.
 #include <mutex>
 
-#include "../../include/pagedattn.h"
+#include "pagedattn.h"
 #include "pa_internal.h"
 
 namespace {
