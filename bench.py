@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
+    ap.add_argument("--qlen", type=int, default=1, help="new query tokens per sequence (multi-token decode)")
     ap.add_argument("--ref-budget", type=float, default=0.0,
                     help="reference arm: seconds of oracle work per step (default min(20, 120 / steps))")
     return ap.parse_args()
@@ -329,7 +330,7 @@ def run_ours(args, wl, world, rank, local, pg):
     dec_avg = sum(dec_ms) / K
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
-    kernel_name = "decode_split" if P else "decode"
+    kernel_name = "decode_multi" if wl.qlen > 1 else ("decode_split" if P else "decode")
     traffic = recorded_traffic(wl.name, kernel_name)
 
     e2e = None
@@ -417,7 +418,7 @@ def main():
     if args.impl == "reference" and rank != 0:
         return
     seed = args.config + 1000 * rank  # replicas draw independent batches
-    wl = W.make_config(args.config, seed=seed)
+    wl = W.make_config(args.config, seed=seed, qlen=args.qlen)
     if args.seqs and args.seqs < wl.S:
         name = "%s_first%d" % (wl.name, args.seqs)
         wl = W.subset(wl, np.arange(args.seqs))

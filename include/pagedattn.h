@@ -121,6 +121,24 @@ PA_API int pa_decode(void *out, const void *q, int32_t q_dtype, int32_t num_seqs
               float scale, float kv_scale, pa_stream_t stream);
 
 /*
+ * pa_decode_multi: decode of num_q_tokens (k) new tokens per sequence at once,
+ * as when a target model verifies k draft tokens in one pass (speculative
+ * decoding: web page "vLLM", speculative decoding paragraph; review §10).
+ * New token j of sequence s sits at position context_lens[s] - k + j (all k
+ * were written to the cache, e.g. by pa_reshape_and_cache with k slots per
+ * sequence) and attends causally to positions 0 .. context_lens[s] - k + j:
+ *   out[s][j][g] = sum_{i <= L-k+j} softmax_i(scale * q[s][j][g] . k_i) v_i
+ *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
+ * A token whose position is negative (k > L) gets a zero output.  The k
+ * tokens of all G query heads of a kv head are served by one CTA as G * k
+ * MMA columns, so G * k must be at most 16.  Other arguments as pa_decode.
+ */
+PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+                           int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                           const pa_cache_desc *cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, float scale, float kv_scale, pa_stream_t stream);
+
+/*
  * Workspace bytes pa_decode_split needs: num_seqs * num_q_heads *
  * ceil(max_context_len / partition_size) * (head_dim + 2) * 4.  Returns 0 for
  * invalid sizes.

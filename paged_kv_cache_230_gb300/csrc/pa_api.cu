@@ -131,6 +131,7 @@ struct DecodeArgs {
   void* out;
   const void* q;
   int32_t q_dtype, num_seqs, num_q_heads;
+  int32_t qlen;
   const void* k_cache;
   const void* v_cache;
   const pa_cache_desc* cache;
@@ -147,7 +148,9 @@ int check_decode(const DecodeArgs& a) {
   if (a.q_dtype != PA_F16 && a.q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (a.cache->kv_dtype != PA_FP8_E4M3 && a.cache->kv_dtype != a.q_dtype) return PA_ERR_UNSUPPORTED;
   if (a.num_q_heads % a.cache->num_kv_heads) return PA_ERR_INVALID_ARG;
-  if (a.num_q_heads / a.cache->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
+  if (a.qlen < 1) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a.num_q_heads / a.cache->num_kv_heads) * a.qlen > pa::kMaxGroup)
+    return PA_ERR_UNSUPPORTED;
   if (!std::isfinite(a.scale)) return PA_ERR_INVALID_ARG;
   rc = check_kv_scale(a.cache->kv_dtype, a.kv_scale);
   if (rc) return rc;
@@ -172,6 +175,7 @@ pa::DecodeParams make_params(const DecodeArgs& a, int* err) {
   p.G = a.num_q_heads / a.cache->num_kv_heads;
   p.bs = a.cache->block_size;
   p.maxB = a.max_blocks_per_seq;
+  p.qlen = a.qlen;
   p.q_dtype = a.q_dtype;
   p.partition_size = 0;
   p.Pmax = 1;
@@ -260,7 +264,26 @@ int pa_decode(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32
               const void* v_cache, const pa_cache_desc* cache, const int32_t* block_tables,
               int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, float kv_scale,
               pa_stream_t stream) {
-  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, 1, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, kv_scale};
+  int rc = check_decode(a);
+  if (rc || num_seqs == 0) return rc;
+  if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
+    return rc;
+  const pa::DecodeParams p = make_params(a, err);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st), st);
+}
+
+int pa_decode_multi(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+                    int32_t num_q_heads, const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    float scale, float kv_scale, pa_stream_t stream) {
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
   int rc = check_decode(a);
   if (rc || num_seqs == 0) return rc;
@@ -287,7 +310,7 @@ int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
                     const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
                     float scale, float kv_scale, int32_t max_context_len, int32_t partition_size, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream) {
-  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, 1, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
   int rc = check_decode(a);
   if (rc) return rc;

@@ -259,6 +259,12 @@ __device__ __noinline__ static int seq_of_rank(const int32_t* __restrict__ conte
   return min(max(sel[2], 0), S - 1);
 }
 
+// Query columns of a CTA: column n is query token n / G (of qlen new tokens)
+// and query head h * G + n % G; its row in q / out [S, qlen, Hq, D].
+__device__ __forceinline__ int64_t query_row(const DecodeParams& p, int s, int h, int n) {
+  return (static_cast<int64_t>(s) * p.qlen + n / p.G) * p.Hq + h * p.G + n % p.G;
+}
+
 // Combination of the consumer warps' partial states for one segment (the
 // whole token range, or one 512-token partition in the split variant).
 // Every warp has written its (m, l) per head to ml[w][g]; the warps then add
@@ -282,7 +288,7 @@ struct SegInfo {
 
 template <int D, int NG, class AddMine>
 __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, int ctid, float* area,
-                                                 float* carea, float* cml, const float* ml, int64_t qrow0,
+                                                 float* carea, float* cml, const float* ml, int s, int h,
                                                  const SegInfo& si, float vscale, AddMine add_mine) {
   constexpr int NCW = kConsumerWarps;
   named_bar_sync(1, NCW * 32);  // every warp's (m, l) is visible
@@ -293,7 +299,7 @@ __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, 
   }
   const float* cml_in = cml + ((si.seg + 1) & 1) * NG * 2;  // run state before this segment
   float* cml_out = cml + (si.seg & 1) * NG * 2;
-  for (int idx = ctid; idx < p.G * D; idx += NCW * 32) {
+  for (int idx = ctid; idx < p.G * p.qlen * D; idx += NCW * 32) {
     const int g = idx / D, d = idx % D;
     float M = -CUDART_INF_F;
 #pragma unroll
@@ -304,7 +310,7 @@ __device__ __forceinline__ void segment_epilogue(const DecodeParams& p, int cw, 
       for (int w = 0; w < NCW; ++w) lsum += ml[(w * NG + g) * 2 + 1] * ex2(ml[(w * NG + g) * 2] - M);
     }
     float acc = area[g * D + d] * vscale;
-    const int64_t row = qrow0 + g;
+    const int64_t row = query_row(p, s, h, g);
     if (si.split) {
       // fold this partition into the run: log-sum-exp of (run so far, partition)
       if (si.seg > 0) {
@@ -478,12 +484,12 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
   // ========================= consumer warps =========================
   const int cw = warp;
   const int ctid = tid;  // 0..NCW*32-1
-  const int64_t qrow0 = static_cast<int64_t>(s) * p.Hq + h * p.G;
+  const int ncol = p.G * p.qlen;  // query columns (heads x new tokens)
   float qmax = 0.f;
   for (int idx = ctid; idx < NG * D; idx += NCW * 32) {
     const int g = idx / D, d = idx % D;
     float v = 0.f;
-    if (g < p.G) v = load_q(p.q, (qrow0 + g) * D + d, p.q_dtype);
+    if (g < ncol) v = load_q(p.q, query_row(p, s, h, g) * D + d, p.q_dtype);
     qbuf[idx] = v;
     qmax = fmaxf(qmax, fabsf(v));
   }
@@ -561,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           }
         }
       }
-      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, qrow0, SegInfo{seg, last, split, final_out, chunk},
+      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, chunk},
                               vscale, [&](bool first) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -585,6 +591,16 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
         }
       });
     };
+    // token limit of each of this lane's query columns: new token j of qlen
+    // sits at position L - qlen + j and attends to positions up to itself
+    int lim[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int n = nt * 8 + 2 * qc + c2;
+        lim[nt][c2] = n < ncol ? min(tok_end, L - p.qlen + n / p.G + 1) : tok_end;
+      }
     reset();
     int seg_t = 0;  // tiles done in the current segment
     for (int t = 0; t < ntiles; ++t) {
@@ -593,7 +609,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
-      const int n_valid = min(16, tok_end - (tok_begin + t * TILE + row0));
+      const int slice0 = tok_begin + t * TILE + row0;  // first token of this warp's 16
+      const int n_valid = min(16, tok_end - slice0);
       if (n_valid > 0) {
         const uint32_t kst = ring_u32 + stage * Gm::STAGE_BYTES;
         const uint32_t vst = kst + Gm::HALF_BYTES;
@@ -639,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int row = qr + (e >= 2 ? 8 : 0);
-            sv[e] = row < n_valid ? sacc[nt][e] * qk_mult : -CUDART_INF_F;
+            sv[e] = slice0 + row < lim[nt][e & 1] ? sacc[nt][e] * qk_mult : -CUDART_INF_F;
           }
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
@@ -763,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           ml[(cw * NG + g) * 2 + 1] = l_run[g];
         }
       }
-      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, qrow0, SegInfo{seg, last, split, final_out, chunk},
+      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, chunk},
                               vscale, [&](bool first) {
         if (grp == 0) {
 #pragma unroll
@@ -886,8 +903,8 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodePa
   __shared__ float wsh[kMergeMaxParts];
   __shared__ float red[kMergeThreads / 32];
   __shared__ float acc_sh[NGRP][D];
-  const int row = blockIdx.x;  // s * Hq + query head
-  const int s = row / p.Hq;
+  const int row = blockIdx.x;  // (s * qlen + new token) * Hq + query head
+  const int s = row / (p.Hq * p.qlen);
   const int lmax = min(p.maxB * p.bs, p.Pmax * p.partition_size);
   const int L = min(max(p.context_lens[s], 0), lmax);
   const int nparts = (L + p.partition_size - 1) / p.partition_size;
@@ -939,9 +956,10 @@ cudaError_t launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUte
 template <int KV, int D>
 cudaError_t launch_for_d(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          cudaStream_t st) {
-  if (p.G == 1) return launch_one<KV, D, false, 1>(p, tmK, tmV, st);
-  if (p.G <= 3) return launch_one<KV, D, false, 3>(p, tmK, tmV, st);
-  if (p.G <= 8) return launch_one<KV, D, true, 8>(p, tmK, tmV, st);
+  const int ncol = p.G * p.qlen;
+  if (p.qlen == 1 && p.G == 1) return launch_one<KV, D, false, 1>(p, tmK, tmV, st);
+  if (p.qlen == 1 && p.G <= 3) return launch_one<KV, D, false, 3>(p, tmK, tmV, st);
+  if (ncol <= 8) return launch_one<KV, D, true, 8>(p, tmK, tmV, st);
   return launch_one<KV, D, true, 16>(p, tmK, tmV, st);
 }
 

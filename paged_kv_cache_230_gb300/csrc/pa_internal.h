@@ -28,15 +28,16 @@ constexpr int kMaxGroup = 16;                     // largest query group G
 enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
 struct DecodeParams {
-  void* out;                  // [S, Hq, D] of q_dtype
-  const void* q;              // [S, Hq, D] of q_dtype
+  void* out;                  // [S, qlen, Hq, D] of q_dtype
+  const void* q;              // [S, qlen, Hq, D] of q_dtype
   const int32_t* block_tables;  // [S, maxB]
   const int32_t* context_lens;  // [S]
-  float* ws_ml;               // split: [S, Hq, Pmax, 2] (m, l); nullptr without split
-  float* ws_o;                // split: [S, Hq, Pmax, D]
+  float* ws_ml;               // split: [S, qlen, Hq, Pmax, 2] (m, l); nullptr without split
+  float* ws_o;                // split: [S, qlen, Hq, Pmax, D]
   int* err;                   // device error word (PA_DEVERR_* bits)
   int64_t num_blocks;
   int S, Hq, Hkv, G, bs, maxB;
+  int qlen;                   // new query tokens per sequence (1 = one-token decode)
   int q_dtype;
   int partition_size;         // tokens per partition; 0 = whole context per CTA
   int Pmax;                   // partitions per sequence (1 without split)

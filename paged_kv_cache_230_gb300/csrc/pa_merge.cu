@@ -4,7 +4,7 @@
 namespace pa {
 
 cudaError_t launch_lse_merge(const DecodeParams& p, int head_dim, cudaStream_t st) {
-  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.S) * p.Hq);
+  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.S) * p.qlen * p.Hq);
   if (head_dim == 64)
     lse_merge_kernel<64><<<grid, kMergeThreads, 0, st>>>(p);
   else

@@ -60,7 +60,10 @@ class DeviceBatch:
 
     def decode(self) -> torch.Tensor:
         wl = self.wl
-        if self.partition_size:
+        if wl.qlen > 1:
+            pa.decode_multi(self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+                            wl.scale, wl.kv_scale)
+        elif self.partition_size:
             pa.decode_split(self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
                             wl.scale, wl.kv_scale, wl.max_context_len, self.partition_size, self.workspace)
         else:

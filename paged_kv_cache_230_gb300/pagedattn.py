@@ -29,7 +29,8 @@ PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: "workspace",
           -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_split_workspace_size", "pa_decode_split",
+EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split_workspace_size",
+           "pa_decode_split",
            "pa_decode_split_noalloc", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
            "pa_version"]
 
@@ -53,6 +54,8 @@ def _load() -> ctypes.CDLL:
     P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     lib.pa_reshape_and_cache.argtypes = [P, P, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, f32, P]
     lib.pa_decode.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
+    lib.pa_decode_multi.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
+                                    P]
     lib.pa_decode_split_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
     lib.pa_decode_split.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
@@ -64,7 +67,7 @@ def _load() -> ctypes.CDLL:
     lib.pa_set_check_mode.argtypes = [ctypes.c_int]
     lib.pa_get_device_error.argtypes = []
     lib.pa_version.argtypes = []
-    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_noalloc",
+    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split", "pa_decode_split_noalloc",
                  "pa_set_check_mode",
                  "pa_get_device_error", "pa_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -168,6 +171,26 @@ def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
                            _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1],
                            _ptr(context_lens), float(scale), float(kv_scale), _stream(dev))
     _check("pa_decode", rc)
+
+
+def decode_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float = 1.0) -> None:
+    """Decode of k new tokens per sequence, q/out [S, k, Hq, D], causal within the new tokens."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", (torch.float16, torch.bfloat16), 4, dev)
+    _need(out, "out", q.dtype, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S, k, Hq, D = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != S or context_lens.shape[0] != S or D != k_cache.shape[3]:
+        raise ValueError("q/out/block_tables/context_lens shapes disagree")
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_decode_multi(_ptr(out), _ptr(q), _dtype_code(q.dtype), S, k, Hq, _ptr(k_cache), _ptr(v_cache),
+                                 ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                 float(scale), float(kv_scale), _stream(dev))
+    _check("pa_decode_multi", rc)
 
 
 def decode_split_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,

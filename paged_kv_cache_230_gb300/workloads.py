@@ -83,10 +83,12 @@ def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
 class Workload:
     """One decode step's inputs in the library's layouts (all host numpy arrays).
 
-    Layouts: q ``[S, Hq, D]``; key/value (this step's token) ``[S, Hkv, D]``;
+    Layouts: q ``[S, Hq, D]`` (``[S, qlen, Hq, D]`` when qlen > 1); key/value
+    (this step's tokens) ``[S * qlen, Hkv, D]``;
     caches ``[NB, Hkv, bs, D]``; block_tables ``int32 [S, max_blocks]``
     (entries past ceil(L/bs) are -1); context_lens ``int32 [S]`` (includes this
-    step's token); slot_mapping ``int64 [S]``.
+    step's tokens); slot_mapping ``int64 [S * qlen]`` (token j of sequence s at
+    position L - qlen + j; -1 where that position is negative).
 
     For 16-bit caches ``k_cache``/``v_cache`` hold the full pool contents.  For
     FP8 caches they are None and the pool is filled by scattering
@@ -117,6 +119,7 @@ class Workload:
     prefill_value: Optional[np.ndarray] = None
     prefill_slots: Optional[np.ndarray] = None
     partition_size: int = 0
+    qlen: int = 1
     notes: dict = field(default_factory=dict)
 
     @property
@@ -147,12 +150,12 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """KV bytes + q in + out + block-table entries used + context lengths."""
         nblk = int(((self.context_lens.astype(np.int64) + self.bs - 1) // self.bs).sum())
-        return self.kv_bytes() + self.S * self.Hq * self.D * 2 * 2 + nblk * 4 + self.S * 4
+        return self.kv_bytes() + self.S * self.qlen * self.Hq * self.D * 2 * 2 + nblk * 4 + self.S * 4
 
     def scatter_bytes(self) -> int:
         """reshape_and_cache bytes: new K/V rows read + cache rows written + slot ids."""
         rows = int((self.slot_mapping >= 0).sum()) * self.Hkv * self.D
-        return rows * 2 * 2 + rows * 2 * ELEM_BYTES[self.kv_dtype] + self.S * 8
+        return rows * 2 * 2 + rows * 2 * ELEM_BYTES[self.kv_dtype] + len(self.slot_mapping) * 8
 
 
 # ---------------------------------------------------------------------------
@@ -181,12 +184,15 @@ def check_block_table_invariant(block_tables, context_lens, bs, NB, refcount=Non
     return counts
 
 
-def _slots_for_last_token(block_tables, context_lens, bs):
+def _slots_for_last_tokens(block_tables, context_lens, bs, qlen=1):
+    """Slots of the last qlen positions of every context, [S * qlen] (-1 where
+    the position is negative)."""
     L = context_lens.astype(np.int64)
-    rows = np.arange(len(L))
-    last = np.maximum(L - 1, 0)
-    phys = block_tables[rows, last // bs].astype(np.int64)
-    return np.where(L > 0, phys * bs + last % bs, -1)
+    S = len(L)
+    pos = L[:, None] - qlen + np.arange(qlen)[None, :]  # [S, qlen]
+    posc = np.maximum(pos, 0)
+    phys = block_tables[np.arange(S)[:, None], posc // bs].astype(np.int64)
+    return np.where(pos >= 0, phys * bs + posc % bs, -1).reshape(-1)
 
 
 def make_workload(
@@ -207,6 +213,7 @@ def make_workload(
     scale: Optional[float] = None,
     partition_size: int = 0,
     fill_unused: str = "normal",
+    qlen: int = 1,
 ) -> Workload:
     """Builds a seeded workload.
 
@@ -265,18 +272,18 @@ def make_workload(
             bt[s, :k] = perm[nxt:nxt + k]
             nxt += k
 
-    slot_mapping = _slots_for_last_token(bt, L, bs) if S else np.zeros(0, np.int64)
-    q = normal_bits(s_q, (S, Hq, D), q_dtype)
+    slot_mapping = _slots_for_last_tokens(bt, L, bs, qlen) if S else np.zeros(0, np.int64)
+    q = normal_bits(s_q, (S, Hq, D) if qlen == 1 else (S, qlen, Hq, D), q_dtype)
     s_key, s_value = s_new.spawn(2)
-    key = normal_bits(s_key, (S, Hkv, D), q_dtype)
-    value = normal_bits(s_value, (S, Hkv, D), q_dtype)
+    key = normal_bits(s_key, (S * qlen, Hkv, D), q_dtype)
+    value = normal_bits(s_value, (S * qlen, Hkv, D), q_dtype)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
 
     wl = Workload(name=name, S=S, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, q_dtype=q_dtype,
                   kv_dtype=kv_dtype, q=q, key=key, value=value, block_tables=bt,
                   context_lens=L, slot_mapping=slot_mapping.astype(np.int64), scale=float(scale),
-                  partition_size=partition_size)
+                  partition_size=partition_size, qlen=qlen)
 
     if kv_dtype != FP8:
         shape = (NB, Hkv, bs, D)
@@ -284,7 +291,7 @@ def make_workload(
             kc = np.full(shape, 0xFFFF, dtype=np.uint16)
             vc = np.full(shape, 0xFFFF, dtype=np.uint16)
             # live tokens only (all but the one this step writes)
-            live = _live_slots(bt, L - 1, bs)
+            live = _live_slots(bt, L - qlen, bs)
             s_k, s_v = s_kv.spawn(2)
             kd = normal_bits(s_k, (len(live), Hkv, D), kv_dtype)
             vd = normal_bits(s_v, (len(live), Hkv, D), kv_dtype)
@@ -300,7 +307,7 @@ def make_workload(
     else:
         # Every live token (all but the one this step writes) gets 16-bit K/V
         # draws that are scattered into the FP8 pool before the step.
-        live = _live_slots(bt, L - 1, bs)
+        live = _live_slots(bt, L - qlen, bs)
         s_k, s_v = s_pre.spawn(2)
         pk = normal_bits(s_k, (len(live), Hkv, D), q_dtype)
         pv = normal_bits(s_v, (len(live), Hkv, D), q_dtype)
@@ -356,7 +363,7 @@ def config_lengths(idx: int, seed: int) -> np.ndarray:
     raise ValueError(idx)
 
 
-def make_config(idx: int, seed: Optional[int] = None, fill_unused: str = "normal") -> Workload:
+def make_config(idx: int, seed: Optional[int] = None, fill_unused: str = "normal", qlen: int = 1) -> Workload:
     """The five decode workloads:
 
     0 tiny: 4 seqs, 8/8 heads, D 64, fp16, L ~ U{1..200}, pool of 64 blocks.
@@ -368,7 +375,8 @@ def make_config(idx: int, seed: Optional[int] = None, fill_unused: str = "normal
     """
     seed = idx if seed is None else seed
     L = config_lengths(idx, seed)
-    common = dict(name=CONFIG_NAMES[idx], seed=seed, context_lens=L, bs=16, fill_unused=fill_unused)
+    common = dict(name=CONFIG_NAMES[idx] if qlen == 1 else "%s_q%d" % (CONFIG_NAMES[idx], qlen), seed=seed,
+                  context_lens=L, bs=16, fill_unused=fill_unused, qlen=qlen)
     if idx == 0:
         return make_workload(Hq=8, Hkv=8, D=64, q_dtype=F16, kv_dtype=F16, max_blocks=13, NB=64, **common)
     if idx == 1:
@@ -390,9 +398,10 @@ def subset(wl: Workload, seqs) -> Workload:
     out = Workload(**{k: getattr(wl, k) for k in wl.__dataclass_fields__})
     out.S = len(seqs)
     out.q = np.ascontiguousarray(wl.q[seqs])
-    out.key = np.ascontiguousarray(wl.key[seqs])
-    out.value = np.ascontiguousarray(wl.value[seqs])
+    tok = (seqs[:, None] * wl.qlen + np.arange(wl.qlen)[None, :]).reshape(-1)
+    out.key = np.ascontiguousarray(wl.key[tok])
+    out.value = np.ascontiguousarray(wl.value[tok])
     out.block_tables = np.ascontiguousarray(wl.block_tables[seqs])
     out.context_lens = np.ascontiguousarray(wl.context_lens[seqs])
-    out.slot_mapping = np.ascontiguousarray(wl.slot_mapping[seqs])
+    out.slot_mapping = np.ascontiguousarray(wl.slot_mapping[tok])
     return out

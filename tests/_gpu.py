@@ -70,6 +70,8 @@ class OnGpu:
                 self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.q.device)
             pa.decode_split(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale, mcl,
                             partition_size, self.ws)
+        elif wl.qlen > 1:
+            pa.decode_multi(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale)
         else:
             pa.decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale)
         return self.out
@@ -100,8 +102,21 @@ def oracle_pool(wl: W.Workload):
 
 
 def oracle_out(wl: W.Workload, kc, vc, partition_size: int = 0):
-    return oracle.decode(wl.q, wl.q_dtype, kc, vc, wl.kv_dtype, wl.block_tables, wl.context_lens, wl.scale,
-                         wl.kv_scale, partition_size=partition_size)
+    """Oracle output in the workload's q layout.  With k new tokens per
+    sequence, new token j of sequence s is decoded by the oracle as its own
+    query over the context prefix ending at its position L - k + j (the
+    causal rule), through the same block-table row."""
+    if wl.qlen == 1:
+        return oracle.decode(wl.q, wl.q_dtype, kc, vc, wl.kv_dtype, wl.block_tables, wl.context_lens, wl.scale,
+                             wl.kv_scale, partition_size=partition_size)
+    k = wl.qlen
+    q = wl.q.reshape(wl.S * k, wl.Hq, wl.D)
+    bt = np.repeat(wl.block_tables, k, axis=0)
+    L = (wl.context_lens[:, None] - k + 1 + np.arange(k)[None, :]).reshape(-1)
+    Lc = np.maximum(L, 0).astype(np.int32)
+    out = oracle.decode(q, wl.q_dtype, kc, vc, wl.kv_dtype, bt, Lc, wl.scale, wl.kv_scale,
+                        partition_size=partition_size)
+    return out.reshape(wl.S, k, wl.Hq, wl.D)
 
 
 def out_f64(t: torch.Tensor) -> np.ndarray:

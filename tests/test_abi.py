@@ -25,7 +25,8 @@ def declared_functions():
 
 
 def test_header_declares_the_calls():
-    assert declared_functions() == sorted(["pa_reshape_and_cache", "pa_decode", "pa_decode_split_workspace_size",
+    assert declared_functions() == sorted(["pa_reshape_and_cache", "pa_decode", "pa_decode_multi",
+                                           "pa_decode_split_workspace_size",
                                            "pa_decode_split", "pa_decode_split_noalloc", "pa_status_string",
                                            "pa_set_check_mode", "pa_get_device_error", "pa_version"])
 

@@ -321,3 +321,41 @@ def test_fp8_config_scale_covers_every_value():
     wl = W.make_config(4)
     amax = max(np.abs(W.bits_to_f32(a, "bf16")).max() for a in (wl.prefill_key, wl.prefill_value, wl.key, wl.value))
     assert wl.kv_scale == float(np.float32(amax) / np.float32(448.0))
+
+
+def test_multi_token_reading_is_causal_dense_attention():
+    """The tests' oracle for k new tokens (each new token decoded over the
+    context prefix ending at its own position) equals dense causal attention
+    computed with scipy on the unpaged rows."""
+    from tests import _gpu
+    k = 3
+    wl = W.make_workload(name="t", seed=15, context_lens=[2, 9, 40], Hq=4, Hkv=2, D=16, bs=8, q_dtype="bf16",
+                         kv_dtype="bf16", qlen=k)
+    kc, vc = _filled(wl)
+    got = _gpu.oracle_out(wl, kc, vc)
+    q = W.bits_to_f32(wl.q, "bf16").astype(np.float64)  # [S, k, Hq, D]
+    kd = W.bits_to_f32(kc, "bf16").astype(np.float64)
+    vd = W.bits_to_f32(vc, "bf16").astype(np.float64)
+    for s in range(wl.S):
+        L = int(wl.context_lens[s])
+        i = np.arange(L)
+        phys = wl.block_tables[s, i // wl.bs]
+        for j in range(k):
+            pos = L - k + j
+            for g in range(wl.Hq):
+                if pos < 0:
+                    assert np.all(got[s, j, g] == 0)
+                    continue
+                K = kd[phys, g // wl.G, i % wl.bs, :][: pos + 1]
+                V = vd[phys, g // wl.G, i % wl.bs, :][: pos + 1]
+                p = scipy.special.softmax(wl.scale * (K @ q[s, j, g]))
+                np.testing.assert_allclose(got[s, j, g], p @ V, rtol=1e-12, atol=1e-13)
+    # the scatter writes the k new rows at positions L - k .. L - 1
+    for s in range(wl.S):
+        for j in range(k):
+            pos = int(wl.context_lens[s]) - k + j
+            sl = wl.slot_mapping[s * k + j]
+            if pos < 0:
+                assert sl == -1
+            else:
+                assert sl == wl.block_tables[s, pos // wl.bs] * wl.bs + pos % wl.bs
