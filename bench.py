@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
     ap.add_argument("--qlen", type=int, default=1, help="new query tokens per sequence (multi-token decode)")
+    ap.add_argument("--op", default="decode", choices=["decode", "blocks"],
+                    help="blocks: time copy-on-write block copies and swap-out/in through pinned host memory")
     ap.add_argument("--ref-budget", type=float, default=0.0,
                     help="reference arm: seconds of oracle work per step (default min(20, 120 / steps))")
     return ap.parse_args()
@@ -412,9 +414,60 @@ def e2e_measure(b, wl, dev, K, warm, pg):
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
 
 
+def run_blocks(args, local):
+    """Whole-block moves on the gqa8b pool shape (8 kv heads x 16 tokens x 128
+    channels, bf16: 32 KiB per block per cache): pa_copy_blocks of 4096
+    disjoint (src, dst) pairs, then pa_gather_blocks into pinned host memory
+    and pa_scatter_blocks back from it for 4096 blocks.  GB/s counts bytes
+    read plus bytes written."""
+    import torch
+    from paged_kv_cache_230_gb300 import build as _build
+    _build.build()
+    from paged_kv_cache_230_gb300 import pagedattn as pa
+    torch.cuda.set_device(local)
+    NB, Hkv, bs, D, n = 16384, 8, 16, 128, 4096
+    kc = torch.randn((NB, Hkv, bs, D), device="cuda").to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    perm = torch.randperm(NB, device="cuda")
+    pairs = torch.stack([perm[:n], perm[n:2 * n]], dim=1).contiguous()
+    ids = perm[2 * n:3 * n].contiguous()
+    host = torch.empty((n, 2, Hkv, bs, D), dtype=torch.bfloat16, pin_memory=True)
+    block = Hkv * bs * D * 2
+    moved = 2 * n * block  # K and V blocks per call
+    res = {}
+    for name, fn in (("copy_blocks", lambda: pa.copy_blocks(kc, vc, pairs)),
+                     ("gather_to_host", lambda: pa.gather_blocks(host, kc, vc, ids)),
+                     ("scatter_from_host", lambda: pa.scatter_blocks(kc, vc, host, ids))):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        K = max(1, min(args.steps, 200))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / K
+        res[name] = {"us": us, "gbs": 2 * moved / (us * 1e-6) / 1e9}
+    peak, kind = measured_hbm_peak()
+    line = {"metric": "block copy GB/s (read + write)", "value": res["copy_blocks"]["gbs"], "unit": "GB/s",
+            "n_gpus": 1, "steps": min(args.steps, 200), "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "blocks_gqa8b_pool", "blocks_per_call": n, "block_bytes_per_cache": block},
+            "ops": res,
+            "roofline": {"bound": "hbm", "achieved": res["copy_blocks"]["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": res["copy_blocks"]["gbs"] / peak, "peak_source": kind, "kernel": "pa_copy_blocks"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local, pg = dist_setup()
+    if args.op == "blocks":
+        if rank == 0:
+            run_blocks(args, local)
+        return
     if args.impl == "reference" and rank != 0:
         return
     seed = args.config + 1000 * rank  # replicas draw independent batches

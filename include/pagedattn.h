@@ -68,7 +68,9 @@ typedef enum {
     PA_ERR_WORKSPACE = -3,   /* split workspace missing or too small                 */
     PA_ERR_CUDA = -4,        /* a CUDA runtime/driver call or launch failed          */
     PA_ERR_BAD_INDEX = -5,   /* check mode: a kernel saw an out-of-range index       */
-    PA_ERR_TIMEOUT = -6      /* a kernel gave up waiting on its own copy pipeline    */
+    PA_ERR_TIMEOUT = -6,     /* a kernel gave up waiting on its own copy pipeline    */
+    PA_ERR_OUT_OF_BLOCKS = -7, /* block manager: not enough free blocks (nothing changed) */
+    PA_ERR_NOT_FOUND = -8    /* block manager: unknown sequence id, or id already used */
 } pa_status;
 
 /* Device error word bits (pa_get_device_error). */
@@ -190,6 +192,64 @@ PA_API int pa_decode_split_noalloc(void *out, const void *q, int32_t q_dtype, in
                                    int32_t max_blocks_per_seq, const int32_t *context_lens, float scale,
                                    float kv_scale, int32_t max_context_len, int32_t partition_size,
                                    pa_stream_t stream);
+
+/*
+ * Whole-block moves on the pool (all kv heads of a block, K and V).  One
+ * block of one cache is num_kv_heads * block_size * head_dim * eb bytes.
+ * Index arrays are int64 and, like every buffer here, device-accessible
+ * (device memory, or pinned host memory mapped into the device's address
+ * space, which is how blocks are swapped to and from the host).  Ids outside
+ * the pool are skipped and recorded (PA_DEVERR_BLOCK_ID).  The index array
+ * and the buffer are checked with cudaPointerGetAttributes before anything is
+ * launched: pinned host memory is used through its device mapping, and
+ * memory the device cannot reach returns PA_ERR_INVALID_ARG.
+ *
+ * pa_copy_blocks: for each pair (src, dst) of block_pairs[num_pairs][2],
+ *   k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src].  Used for
+ *   copy-on-write of a shared, partially filled last block (review §6, §9).
+ *   No dst may equal another pair's src or dst.
+ * pa_gather_blocks: dst[i][0] = k_cache[block_ids[i]], dst[i][1] =
+ *   v_cache[block_ids[i]]; dst is [num][2][Hkv][bs][D] of the cache dtype,
+ *   16-byte aligned (swap-out to host memory for preemption, review §9).
+ * pa_scatter_blocks: the inverse (swap-in).
+ */
+PA_API int pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc *cache, const int64_t *block_pairs,
+                          int32_t num_pairs, pa_stream_t stream);
+PA_API int pa_gather_blocks(void *dst, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+                            const int64_t *block_ids, int32_t num, pa_stream_t stream);
+PA_API int pa_scatter_blocks(void *k_cache, void *v_cache, const pa_cache_desc *cache, const void *src,
+                             const int64_t *block_ids, int32_t num, pa_stream_t stream);
+
+/*
+ * Host block manager (no device work, not thread-safe: one owner, as the
+ * scheduler owns block tables in the review, §6).  Physical blocks come from
+ * a free list; a sequence's table only grows; pa_bm_fork shares every block
+ * of the parent with the child (a pointer update: reference counts rise, no
+ * data moves); pa_bm_append_tokens returns the slot of each new token and,
+ * when the sequence's last block is shared and partially filled, first moves
+ * the sequence to a private copy of it and reports the (src, dst) pair that
+ * the caller copies with pa_copy_blocks.  A full shared block is never
+ * copied: the next token starts a fresh block.  Calls that would need more
+ * free blocks than exist change nothing and return PA_ERR_OUT_OF_BLOCKS.
+ */
+typedef struct pa_block_manager pa_block_manager;
+PA_API pa_block_manager *pa_bm_create(int64_t num_blocks, int32_t block_size);  /* NULL on bad sizes */
+PA_API void pa_bm_destroy(pa_block_manager *bm);
+PA_API int pa_bm_add_sequence(pa_block_manager *bm, int64_t seq_id, int64_t num_tokens);
+PA_API int pa_bm_fork(pa_block_manager *bm, int64_t parent_id, int64_t child_id);
+PA_API int pa_bm_append_tokens(pa_block_manager *bm, int64_t seq_id, int32_t num_new, int64_t *slots_out,
+                               int64_t *cow_pair_out /* [2] */, int32_t *num_cow_out);
+PA_API int pa_bm_free_sequence(pa_block_manager *bm, int64_t seq_id);
+PA_API int pa_bm_block_table(const pa_block_manager *bm, int64_t seq_id, int32_t *out, int32_t capacity,
+                             int32_t *num_blocks_out, int64_t *num_tokens_out);
+PA_API int64_t pa_bm_num_free_blocks(const pa_block_manager *bm);
+PA_API int32_t pa_bm_refcount(const pa_block_manager *bm, int64_t block);  /* -1 for a bad id */
+/* Unused slots summed over all sequences (each holds at most block_size - 1). */
+PA_API int64_t pa_bm_tail_waste(const pa_block_manager *bm);
+/* Violations of the block invariant (0 = consistent): refcount equals the
+ * number of table entries naming the block, free exactly when unreferenced,
+ * no block twice in one table, ceil(tokens / block_size) blocks per table. */
+PA_API int64_t pa_bm_check(const pa_block_manager *bm);
 
 /* Static description of a status code. */
 PA_API const char *pa_status_string(int status);

@@ -8,5 +8,5 @@ defined.
 from .oracle import (  # noqa: F401
     F16, BF16, E4M3, build, lib, max_threads,
     f16_to_double, bf16_to_double, decode16, e4m3_to_double, float_to_e4m3,
-    round_out, reshape_and_cache, decode, attend_range,
+    round_out, reshape_and_cache, decode, attend_range, copy_blocks, gather_blocks, scatter_blocks,
 )

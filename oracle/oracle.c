@@ -464,6 +464,62 @@ void orc_round_array(const double *x, uint16_t *out, int64_t n, int dtype)
         out[i] = dtype == ORC_F16 ? orc_double_to_f16(x[i]) : orc_double_to_bf16(x[i]);
 }
 
+/* ------------------------------------------------------------------ */
+/* whole-block moves                                                   */
+/* ------------------------------------------------------------------ */
+
+/* Block b of a cache is bytes [b * block_bytes, (b + 1) * block_bytes).
+ * Copy: for each pair in order, cache[dst] = cache[src] (K and V).
+ * Gather: buf[i] = (k[ids[i]], v[ids[i]]).  Scatter: the inverse.
+ * Ids outside [0, num_blocks) are skipped; each returns how many it skipped. */
+int64_t orc_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, int64_t block_bytes, const int64_t *pairs, int64_t n,
+                        int64_t num_blocks)
+{
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        memmove(k_cache + dst * block_bytes, k_cache + src * block_bytes, (size_t)block_bytes);
+        memmove(v_cache + dst * block_bytes, v_cache + src * block_bytes, (size_t)block_bytes);
+    }
+    return bad;
+}
+
+int64_t orc_gather_blocks(uint8_t *buf, const uint8_t *k_cache, const uint8_t *v_cache, int64_t block_bytes,
+                          const int64_t *ids, int64_t n, int64_t num_blocks)
+{
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t b = ids[i];
+        if (b < 0 || b >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        memcpy(buf + (2 * i) * block_bytes, k_cache + b * block_bytes, (size_t)block_bytes);
+        memcpy(buf + (2 * i + 1) * block_bytes, v_cache + b * block_bytes, (size_t)block_bytes);
+    }
+    return bad;
+}
+
+int64_t orc_scatter_blocks(uint8_t *k_cache, uint8_t *v_cache, const uint8_t *buf, int64_t block_bytes,
+                           const int64_t *ids, int64_t n, int64_t num_blocks)
+{
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t b = ids[i];
+        if (b < 0 || b >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        memcpy(k_cache + b * block_bytes, buf + (2 * i) * block_bytes, (size_t)block_bytes);
+        memcpy(v_cache + b * block_bytes, buf + (2 * i + 1) * block_bytes, (size_t)block_bytes);
+    }
+    return bad;
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

@@ -69,6 +69,13 @@ def lib():
             L.orc_e4m3_encode_array.argtypes = [P, P, i64]
             L.orc_round_array.argtypes = [P, P, i64, i32]
             L.orc_max_threads.restype = i32
+            for fn in ("orc_copy_blocks",):
+                getattr(L, fn).argtypes = [P, P, i64, P, i64, i64]
+                getattr(L, fn).restype = i64
+            L.orc_gather_blocks.argtypes = [P, P, P, i64, P, i64, i64]
+            L.orc_gather_blocks.restype = i64
+            L.orc_scatter_blocks.argtypes = [P, P, P, i64, P, i64, i64]
+            L.orc_scatter_blocks.restype = i64
             L.orc_init()
             _lib = L
     return _lib
@@ -175,3 +182,31 @@ def attend_range(q, q_dtype, k_cache, v_cache, cache_dtype, block_tables, scale,
                            _CODES[cache_dtype], NB, bs, _ptr(bt), bt.shape[1], float(scale),
                            float(kv_scale), int(s), int(g), int(t0), int(t1))
     return m.value, l.value, o
+
+
+def _block_bytes(cache):
+    return int(cache[0].nbytes)
+
+
+def copy_blocks(k_cache, v_cache, pairs) -> int:
+    """In place: cache[dst] = cache[src] for each (src, dst) row, in order."""
+    pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    return int(lib().orc_copy_blocks(_ptr(k_cache), _ptr(v_cache), _block_bytes(k_cache), _ptr(pairs),
+                                     len(pairs), k_cache.shape[0]))
+
+
+def gather_blocks(k_cache, v_cache, ids) -> np.ndarray:
+    """[n, 2, *block] buffer of the named blocks (K then V)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    buf = np.zeros((len(ids), 2) + k_cache.shape[1:], k_cache.dtype)
+    lib().orc_gather_blocks(_ptr(buf), _ptr(k_cache), _ptr(v_cache), _block_bytes(k_cache), _ptr(ids), len(ids),
+                            k_cache.shape[0])
+    return buf
+
+
+def scatter_blocks(k_cache, v_cache, buf, ids) -> int:
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    buf = np.ascontiguousarray(buf)
+    return int(lib().orc_scatter_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(buf), _block_bytes(k_cache), _ptr(ids),
+                                        len(ids), k_cache.shape[0]))

@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _deps():
@@ -50,7 +50,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     srcs = _sources()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [exe, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]

@@ -339,6 +339,64 @@ int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
   return finish(e, st);
 }
 
+// Device address through which kernels may touch `p`: device or managed
+// memory as is, pinned host memory through its mapping; false for anything
+// else (for example pageable host memory), so nothing is launched on it.
+static bool device_view(const void* p, void** dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *dev = const_cast<void*>(p);
+    return true;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *dev = a.devicePointer;
+    return true;
+  }
+  return false;
+}
+
+static int block_op(int op, void* buf, void* k_cache, void* v_cache, const pa_cache_desc* cache, const int64_t* ids,
+                    int32_t n, pa_stream_t stream) {
+  int rc = check_cache(cache, k_cache, v_cache);
+  if (rc) return rc;
+  if (n < 0) return PA_ERR_INVALID_ARG;
+  if (n == 0) return PA_OK;
+  if (!ids || (op != 0 && (!buf || !aligned16(buf)))) return PA_ERR_INVALID_ARG;
+  void* ids_dev = nullptr;
+  if (!device_view(ids, &ids_dev)) return PA_ERR_INVALID_ARG;
+  ids = static_cast<const int64_t*>(ids_dev);
+  if (op != 0) {
+    void* buf_dev = nullptr;
+    if (!device_view(buf, &buf_dev)) return PA_ERR_INVALID_ARG;
+    buf = buf_dev;
+  }
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t block_bytes = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim *
+                              elem_bytes(cache->kv_dtype);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(pa::launch_block_op(op, buf, k_cache, v_cache, ids, n, block_bytes, cache->num_blocks, err, st), st);
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc* cache, const int64_t* block_pairs,
+                   int32_t num_pairs, pa_stream_t stream) {
+  return block_op(0, nullptr, k_cache, v_cache, cache, block_pairs, num_pairs, stream);
+}
+
+int pa_gather_blocks(void* dst, const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                     const int64_t* block_ids, int32_t num, pa_stream_t stream) {
+  return block_op(1, dst, const_cast<void*>(k_cache), const_cast<void*>(v_cache), cache, block_ids, num, stream);
+}
+
+int pa_scatter_blocks(void* k_cache, void* v_cache, const pa_cache_desc* cache, const void* src,
+                      const int64_t* block_ids, int32_t num, pa_stream_t stream) {
+  return block_op(2, const_cast<void*>(src), k_cache, v_cache, cache, block_ids, num, stream);
+}
+
 const char* pa_status_string(int status) {
   switch (status) {
     case PA_OK: return "ok";
@@ -348,6 +406,8 @@ const char* pa_status_string(int status) {
     case PA_ERR_CUDA: return "CUDA error";
     case PA_ERR_BAD_INDEX: return "out-of-range index seen by a kernel";
     case PA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case PA_ERR_OUT_OF_BLOCKS: return "not enough free blocks";
+    case PA_ERR_NOT_FOUND: return "unknown or duplicate sequence id";
     default: return "unknown status";
   }
 }

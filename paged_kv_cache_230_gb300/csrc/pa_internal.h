@@ -74,4 +74,9 @@ struct CacheParams {
 
 cudaError_t launch_reshape_and_cache(const CacheParams& p, cudaStream_t st);
 
+// Whole-block moves: op 0 copy (ids = [n][2] pairs), 1 gather into buf,
+// 2 scatter from buf.  block_bytes is one block of one cache (a multiple of 16).
+cudaError_t launch_block_op(int op, void* buf, void* k_cache, void* v_cache, const int64_t* ids, int n,
+                            int64_t block_bytes, int64_t num_blocks, int* err, cudaStream_t st);
+
 }  // namespace pa

@@ -27,11 +27,14 @@ from . import build as _build
 
 PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: "workspace",
-          -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out"}
+          -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out",
+          -7: "not enough free blocks", -8: "unknown or duplicate sequence id"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split_workspace_size",
-           "pa_decode_split",
-           "pa_decode_split_noalloc", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
+           "pa_decode_split", "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
+           "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
+           "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_num_free_blocks", "pa_bm_refcount",
+           "pa_bm_tail_waste", "pa_bm_check", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
            "pa_version"]
 
 
@@ -62,6 +65,30 @@ def _load() -> ctypes.CDLL:
                                     i32, i32, P, ctypes.c_size_t, P]
     lib.pa_decode_split_noalloc.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32,
                                             f32, i32, i32, P]
+    D = ctypes.POINTER(CacheDesc)
+    lib.pa_copy_blocks.argtypes = [P, P, D, P, i32, P]
+    lib.pa_gather_blocks.argtypes = [P, P, P, D, P, i32, P]
+    lib.pa_scatter_blocks.argtypes = [P, P, D, P, P, i32, P]
+    lib.pa_bm_create.argtypes = [i64, i32]
+    lib.pa_bm_create.restype = P
+    lib.pa_bm_destroy.argtypes = [P]
+    lib.pa_bm_destroy.restype = None
+    lib.pa_bm_add_sequence.argtypes = [P, i64, i64]
+    lib.pa_bm_fork.argtypes = [P, i64, i64]
+    lib.pa_bm_append_tokens.argtypes = [P, i64, i32, P, P, P]
+    lib.pa_bm_free_sequence.argtypes = [P, i64]
+    lib.pa_bm_block_table.argtypes = [P, i64, P, i32, P, P]
+    lib.pa_bm_num_free_blocks.argtypes = [P]
+    lib.pa_bm_num_free_blocks.restype = i64
+    lib.pa_bm_refcount.argtypes = [P, i64]
+    lib.pa_bm_refcount.restype = i32
+    lib.pa_bm_tail_waste.argtypes = [P]
+    lib.pa_bm_tail_waste.restype = i64
+    lib.pa_bm_check.argtypes = [P]
+    lib.pa_bm_check.restype = i64
+    for name in ("pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks", "pa_bm_add_sequence", "pa_bm_fork",
+                 "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_block_table"):
+        getattr(lib, name).restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_set_check_mode.argtypes = [ctypes.c_int]
@@ -234,3 +261,116 @@ def get_device_error() -> int:
 
 def status_string(status: int) -> str:
     return lib.pa_status_string(status).decode()
+
+
+# ---------------------------------------------------------------------------
+# whole-block moves
+# ---------------------------------------------------------------------------
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor) -> None:
+    """k/v_cache[dst] = k/v_cache[src] for each row (src, dst) of int64 pairs [n, 2]."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(pairs, "pairs", torch.int64, 2, dev)
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(pairs), pairs.shape[0],
+                                _stream(dev))
+    _check("pa_copy_blocks", rc)
+
+
+def _check_buf(buf: torch.Tensor, k_cache: torch.Tensor, n: int):
+    if not buf.is_contiguous():
+        raise ValueError("buffer must be contiguous")
+    need = n * 2 * k_cache[0].numel() * k_cache.element_size()
+    if buf.numel() * buf.element_size() < need:
+        raise ValueError("buffer holds %d bytes, %d needed" % (buf.numel() * buf.element_size(), need))
+    if not (buf.is_cuda or buf.is_pinned()):
+        raise ValueError("buffer must be device memory or pinned host memory")
+
+
+def gather_blocks(dst: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, ids: torch.Tensor) -> None:
+    """dst[i] = (k_cache[ids[i]], v_cache[ids[i]]); dst is device memory or pinned host memory."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(ids, "ids", torch.int64, 1, dev)
+    _check_buf(dst, k_cache, ids.shape[0])
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_gather_blocks(_ptr(dst), _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(ids),
+                                  ids.shape[0], _stream(dev))
+    _check("pa_gather_blocks", rc)
+
+
+def scatter_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, ids: torch.Tensor) -> None:
+    """(k_cache[ids[i]], v_cache[ids[i]]) = src[i]; src is device memory or pinned host memory."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(ids, "ids", torch.int64, 1, dev)
+    _check_buf(src, k_cache, ids.shape[0])
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_scatter_blocks(_ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(src), _ptr(ids),
+                                   ids.shape[0], _stream(dev))
+    _check("pa_scatter_blocks", rc)
+
+
+# ---------------------------------------------------------------------------
+# host block manager
+# ---------------------------------------------------------------------------
+
+class BlockManager:
+    """Owner of a pool's free list, block tables and reference counts (the
+    native manager in the library; no device work)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._h = lib.pa_bm_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise ValueError("bad pool size")
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib.pa_bm_destroy(h)
+            self._h = None
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> None:
+        _check("pa_bm_add_sequence", lib.pa_bm_add_sequence(self._h, seq_id, num_tokens))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pa_bm_fork", lib.pa_bm_fork(self._h, parent, child))
+
+    def append_tokens(self, seq_id: int, n: int):
+        """Returns (slots [n], copy-on-write pair (src, dst) or None)."""
+        slots = (ctypes.c_int64 * max(n, 1))()
+        pair = (ctypes.c_int64 * 2)()
+        ncow = ctypes.c_int32()
+        _check("pa_bm_append_tokens", lib.pa_bm_append_tokens(self._h, seq_id, n, slots, pair, ctypes.byref(ncow)))
+        return [slots[i] for i in range(n)], ((pair[0], pair[1]) if ncow.value else None)
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check("pa_bm_free_sequence", lib.pa_bm_free_sequence(self._h, seq_id))
+
+    def block_table(self, seq_id: int):
+        """(list of physical block ids, number of tokens)."""
+        nb, nt = ctypes.c_int32(), ctypes.c_int64()
+        rc = lib.pa_bm_block_table(self._h, seq_id, None, 0, ctypes.byref(nb), ctypes.byref(nt))
+        if rc == -8:
+            _check("pa_bm_block_table", rc)
+        buf = (ctypes.c_int32 * max(nb.value, 1))()
+        _check("pa_bm_block_table", lib.pa_bm_block_table(self._h, seq_id, buf, nb.value, ctypes.byref(nb),
+                                                          ctypes.byref(nt)))
+        return [buf[i] for i in range(nb.value)], nt.value
+
+    def num_free_blocks(self) -> int:
+        return int(lib.pa_bm_num_free_blocks(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(lib.pa_bm_refcount(self._h, block))
+
+    def tail_waste(self) -> int:
+        return int(lib.pa_bm_tail_waste(self._h))
+
+    def check(self) -> int:
+        return int(lib.pa_bm_check(self._h))

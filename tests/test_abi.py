@@ -24,11 +24,10 @@ def declared_functions():
     return sorted(set(re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)))
 
 
-def test_header_declares_the_calls():
-    assert declared_functions() == sorted(["pa_reshape_and_cache", "pa_decode", "pa_decode_multi",
-                                           "pa_decode_split_workspace_size",
-                                           "pa_decode_split", "pa_decode_split_noalloc", "pa_status_string",
-                                           "pa_set_check_mode", "pa_get_device_error", "pa_version"])
+def test_header_declares_the_calls(pa):
+    assert declared_functions() == sorted(pa.EXPORTS)
+    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_workspace_size"):
+        assert name in declared_functions()
 
 
 def test_library_exports_every_declared_symbol(pa):
