@@ -175,10 +175,15 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+DECODE_SOURCES = ("pa_decode.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_decode_f16.cu", "pa_decode_bf16.cu",
+                  "pa_decode_fp8.cu")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the sources the decode kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_230_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

@@ -141,6 +141,22 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
                            const int32_t *context_lens, float scale, float kv_scale, pa_stream_t stream);
 
 /*
+ * pa_prefill: the same causal attention as pa_decode_multi for a chunk of C =
+ * num_q_tokens new tokens per sequence (positions L - C .. L - 1 of each
+ * context; chunked prefill, review §10 table), computed on the tensor cores
+ * with tcgen05 MMAs and tensor-memory accumulators for long chunks: prefill is
+ * the compute-bound phase (review §7).  One CTA per (sequence, query head,
+ * 128 query tokens) streams 128-token K/V tiles through the block table.
+ *   out, q   [num_seqs, num_q_tokens, num_q_heads, 128] of q_dtype
+ * Supported: head_dim 128, 16-bit caches of the q dtype, block size 8, 16 or
+ * 32.  Other arguments as pa_decode (no kv_scale: 16-bit caches only).
+ */
+PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+                      int32_t num_q_heads, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                      float scale, pa_stream_t stream);
+
+/*
  * Workspace bytes pa_decode_split needs: num_seqs * num_q_heads *
  * ceil(max_context_len / partition_size) * (head_dim + 2) * 4.  Returns 0 for
  * invalid sizes.

@@ -8,6 +8,7 @@
 
 #include "pagedattn.h"
 #include "pa_internal.h"
+#include "pa_prefill.h"
 
 namespace {
 
@@ -296,6 +297,58 @@ int pa_decode_multi(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
   const pa::DecodeParams p = make_params(a, err);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return finish(launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st), st);
+}
+
+int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+               int32_t num_q_heads, const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+               const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens, float scale,
+               pa_stream_t stream) {
+  int rc = check_cache(cache, k_cache, v_cache);
+  if (rc) return rc;
+  if (num_seqs < 0 || num_q_tokens < 1 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != q_dtype || cache->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads % cache->num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_blocks_per_seq) * cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !block_tables || !context_lens || !aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_tokens;
+  const int64_t nqt = (num_q_tokens + pa::kPfRows - 1) / pa::kPfRows;
+  if (rows > UINT32_MAX || nqt * num_q_heads * num_seqs > INT32_MAX) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
+    return rc;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  // q as {128 channels, heads, tokens}; box = 64 channels x 1 head x 128 tokens
+  const cuuint64_t dims[3] = {128, cuuint64_t(num_q_heads), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {256, cuuint64_t(num_q_heads) * 256};
+  const cuuint32_t box[3] = {64, 1, cuuint32_t(pa::kPfRows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_CUDA;
+  pa::PrefillParams p{};
+  p.out = out;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.err = err;
+  p.num_blocks = cache->num_blocks;
+  p.S = num_seqs;
+  p.C = num_q_tokens;
+  p.Hq = num_q_heads;
+  p.Hkv = cache->num_kv_heads;
+  p.G = num_q_heads / cache->num_kv_heads;
+  p.bs = cache->block_size;
+  p.maxB = max_blocks_per_seq;
+  p.bf16 = q_dtype == PA_BF16 ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(pa::launch_prefill(p, tq, tk, tv, st), st);
 }
 
 size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,

@@ -1,0 +1,31 @@
+// Internal interface of the paged prefill kernel (tcgen05 path).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kPfRows = 128;     // query rows per CTA (MMA M, TMEM lanes)
+constexpr int kPfTile = 128;     // KV tokens per tile (MMA N of S, K of P.V)
+constexpr int kPfStages = 2;     // K/V tiles in flight
+constexpr int kPfThreads = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
+
+struct PrefillParams {
+  void* out;                    // [S, C, Hq, 128] of the cache dtype
+  const int32_t* block_tables;  // [S, maxB]
+  const int32_t* context_lens;  // [S] (includes the C new tokens)
+  int* err;                     // device error word
+  int64_t num_blocks;
+  int S, C, Hq, Hkv, G, bs, maxB;
+  int bf16;                     // 1: bf16 operands, 0: f16
+  float scale_log2;             // softmax scale * log2(e)
+};
+
+// tmQ: 3-D map over q {128 channels, Hq, S*C tokens}, box {64, 1, 128};
+// tmK/tmV: the caches' 4-D maps (box {64, bs, 1, 1}), 128-byte swizzle.
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, cudaStream_t st);
+
+}  // namespace pa

@@ -30,7 +30,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: 
           -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out",
           -7: "not enough free blocks", -8: "unknown or duplicate sequence id"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split_workspace_size",
+EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill", "pa_decode_split_workspace_size",
            "pa_decode_split", "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
            "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_num_free_blocks", "pa_bm_refcount",
@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
     lib.pa_decode_multi.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
                                     P]
+    lib.pa_prefill.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, P]
+    lib.pa_prefill.restype = ctypes.c_int
     lib.pa_decode_split_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
     lib.pa_decode_split.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
@@ -218,6 +220,26 @@ def decode_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
                                  ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                                  float(scale), float(kv_scale), _stream(dev))
     _check("pa_decode_multi", rc)
+
+
+def prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float) -> None:
+    """Chunked prefill on the tensor cores: q/out [S, C, Hq, 128], causal over the paged context."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", (torch.float16, torch.bfloat16), 4, dev)
+    _need(out, "out", q.dtype, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S, C, Hq, D = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != S or context_lens.shape[0] != S or D != k_cache.shape[3]:
+        raise ValueError("q/out/block_tables/context_lens shapes disagree")
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_prefill(_ptr(out), _ptr(q), _dtype_code(q.dtype), S, C, Hq, _ptr(k_cache), _ptr(v_cache),
+                            ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                            float(scale), _stream(dev))
+    _check("pa_prefill", rc)
 
 
 def decode_split_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,
