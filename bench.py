@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
     ap.add_argument("--qlen", type=int, default=1, help="new query tokens per sequence (multi-token decode)")
-    ap.add_argument("--op", default="decode", choices=["decode", "blocks"],
+    ap.add_argument("--op", default="decode", choices=["decode", "blocks", "prefill"],
                     help="blocks: time copy-on-write block copies and swap-out/in through pinned host memory")
     ap.add_argument("--ref-budget", type=float, default=0.0,
                     help="reference arm: seconds of oracle work per step (default min(20, 120 / steps))")
@@ -466,12 +466,68 @@ def run_blocks(args, local):
     print(json.dumps(line), flush=True)
 
 
+def measured_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, local):
+    """Chunked prefill of a GQA 8B-shaped batch through pa_prefill: by default
+    16 sequences, each with a chunk of 2048 new tokens at the end of a
+    4096-token context (32/8 heads, head_dim 128, bf16, block size 16);
+    --seqs and --qlen change the batch and the chunk (context = 2 x chunk).
+    TFLOP/s counts the causal work only: 4 * D * Hq * sum over query rows of
+    (position + 1)."""
+    import torch
+    from paged_kv_cache_230_gb300 import build as _build
+    _build.build()
+    from paged_kv_cache_230_gb300 import pagedattn as pa
+    from paged_kv_cache_230_gb300.device import DeviceBatch
+    torch.cuda.set_device(local)
+    S = args.seqs if args.seqs > 0 else 16
+    C = args.qlen if args.qlen > 1 else 2048
+    L = 2 * C
+    wl = W.make_workload(name="prefill_gqa8b", seed=7, context_lens=[L] * S, Hq=32, Hkv=8, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=C)
+    b = DeviceBatch(wl, "cuda")
+    pos = np.arange(L - C, L, dtype=np.float64)
+    flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())
+
+    def run():
+        pa.prefill(b.out, b.q, b.k_cache, b.v_cache, b.block_tables, b.context_lens, wl.scale)
+
+    for _ in range(max(3, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / K
+    tflops = flops / (us * 1e-6) / 1e12
+    peak, kind = measured_tensor_peak()
+    line = {"metric": "paged prefill attention TFLOP/s (causal FLOPs)", "value": tflops, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": K, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": wl.name, "num_seqs": S, "chunk": C, "context": L,
+                                            "q_heads": 32, "kv_heads": 8, "head_dim": 128},
+            "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6),
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_source": kind, "kernel": "pa_prefill"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local, pg = dist_setup()
-    if args.op == "blocks":
+    if args.op in ("blocks", "prefill"):
         if rank == 0:
-            run_blocks(args, local)
+            (run_blocks if args.op == "blocks" else run_prefill)(args, local)
         return
     if args.impl == "reference" and rank != 0:
         return
