@@ -4,19 +4,23 @@
 // the block table (prefill is the compute-bound phase of the review's §7;
 // chunked prefill interleaves such chunks with decode, §10 table).
 //
-// CTA = (sequence, query head, 128 query rows); 6 warps:
-//   warp 4  TMA: the q tile once, then 128-token K and V tiles, block by
-//           block through the block table, into a 2-stage ring (128-byte
-//           swizzle, the canonical K-major layout of the MMA operands);
+// CTA = (sequence, query head, 128 query rows); 7 warps:
+//   warps 4 and 6  TMA: the q tile once, then 128-token K (warp 4) and V
+//           (warp 6) tiles, block by block through the block table, each
+//           into its own 2-stage ring (128-byte swizzle, the canonical
+//           K-major layout of the MMA operands); K buffers are released when
+//           QK^T completes, V buffers when P.V completes;
 //   warp 5  one thread issues tcgen05.mma: S = Q K^T (M = 128 rows, N = 128
-//           tokens, K = 128 channels) into tensor memory, then, once the
-//           probabilities are ready, O += P V (N = 128 channels, K = 128
-//           tokens, V read channel-major) into a second TMEM region;
+//           tokens, K = 128 channels) into one of two TMEM score buffers
+//           (the next tile's scores are computed while this tile's softmax
+//           runs), then, once the probabilities are ready, O += P V (N = 128
+//           channels, K = 128 tokens, V read channel-major) into a third;
 //   warps 0-3  one thread per query row (= TMEM lane): reads its S row with
 //           tcgen05.ld, applies the causal mask and the online softmax in
 //           base 2 (no cross-thread reduction), writes P as 16-bit values to
-//           shared memory in the A-operand layout, rescales its O row in TMEM
-//           when the running max moved, and at the end writes O / l.
+//           shared memory in the A-operand layout (two buffers), rescales its
+//           O row in TMEM when its reference max moved by more than 2^8, and
+//           at the end writes O / l.
 // Every mbarrier wait gives up after about one second (error bit set).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,10 +42,13 @@ constexpr int kSegBytes = kPfTile * 128;  // 64 channels (128 B) of 128 rows
 constexpr int kTileBytes = 2 * kSegBytes;  // 128 rows x 128 channels x 2 B
 constexpr int kQOff = 0;
 constexpr int kKVOff = kQOff + kTileBytes;                    // stage st: K at +2*st*tile, V after it
-constexpr int kPOff = kKVOff + kPfStages * 2 * kTileBytes;   // probabilities, A operand of P.V
-constexpr int kBarOff = kPOff + kTileBytes;                   // 8 mbarriers + TMEM address slot
-constexpr int kSmemBytes = 1024 + kBarOff + 128;
-constexpr uint32_t kTmemCols = 256;  // S in columns [0, 128), O in [128, 256)
+constexpr int kPOff = kKVOff + kPfStages * 2 * kTileBytes;   // 2 buffers of P, A operand of P.V
+constexpr int kBarOff = kPOff + 2 * kTileBytes;
+constexpr int kSmemBytes = 1024 + kBarOff + 128;  // 15 mbarriers + TMEM address slot
+constexpr uint32_t kTmemCols = 512;  // S buffers in columns [0, 128) and [128, 256), O in [256, 384)
+// A row's reference max moves only when the tile max exceeds it by more than
+// this (base 2): probabilities then stay below 2^8 and O is rescaled rarely.
+constexpr float kRescaleThreshold = 8.f;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -63,11 +70,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t base = smem_u32(smem);
-  const uint32_t q_s = base + kQOff, p_s = base + kPOff;
+  const uint32_t q_s = base + kQOff, p_s0 = base + kPOff;
   const uint32_t bar0 = base + kBarOff;
-  const uint32_t q_full = bar0, kv_full0 = bar0 + 8, kv_empty0 = bar0 + 24;
-  const uint32_t s_full = bar0 + 40, p_full = bar0 + 48, o_done = bar0 + 56;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 64);
+  // per-buffer barriers (index = tile parity), so no wait is on an ambiguous
+  // phase; K and V have their own buffers: K of a tile is released as soon as
+  // its QK^T completes, V only after its P.V
+  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40, v_empty0 = bar0 + 56;
+  const uint32_t s_full0 = bar0 + 72, p_full0 = bar0 + 88, o_done0 = bar0 + 104;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqt = (p.C + kPfRows - 1) / kPfRows;
@@ -90,12 +100,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     mbar_init(q_full, 1);
     for (int st = 0; st < kPfStages; ++st) {
-      mbar_init(kv_full0 + 8 * st, 1);
-      mbar_init(kv_empty0 + 8 * st, 1);
+      mbar_init(k_full0 + 8 * st, 1);
+      mbar_init(k_empty0 + 8 * st, 1);
+      mbar_init(v_full0 + 8 * st, 1);
+      mbar_init(v_empty0 + 8 * st, 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full0 + 8 * b, 1);
+      mbar_init(p_full0 + 8 * b, 128);
+      mbar_init(o_done0 + 8 * b, 1);
+    }
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -106,45 +120,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tS0 = tmem, tO = tmem + 256;
 
-  if (warp == 4) {
-    // ============================ TMA producer ============================
+  if (warp == 4 || warp == 6) {
+    // ===================== TMA producers: warp 4 K, warp 6 V =====================
+    const bool is_k = warp == 4;
     if (ntiles > 0) {
-      if (lane == 0) {
+      if (lane == 0 && is_k) {
         tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
         mbar_arrive_expect_tx(q_full, kTileBytes);
         const int row = s * p.C + i0;
         tma_load_3d(q_s, &tmQ, q_full, 0, h, row);
         tma_load_3d(q_s + kSegBytes, &tmQ, q_full, 64, h, row);
       }
+      if (lane == 0 && !is_k) tma_prefetch_desc(&tmV);
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      const uint32_t full0 = is_k ? k_full0 : v_full0, empty0 = is_k ? k_empty0 : v_empty0;
+      const uint32_t dst0 = base + kKVOff + (is_k ? 0 : kTileBytes);
       const int* bt_row = p.block_tables + static_cast<int64_t>(s) * p.maxB;
       const int bpt = kPfTile / p.bs;
       const int nblk = (kv_len + p.bs - 1) / p.bs;
-      const uint32_t tx_block = static_cast<uint32_t>(2 * p.bs * 256);
+      const uint32_t tx_block = static_cast<uint32_t>(p.bs * 256);
       for (int t = 0; t < ntiles; ++t) {
         const int st = t % kPfStages;
         bool ok = true;
-        if (t >= kPfStages) ok = mbar_wait(kv_empty0 + 8 * st, ((t / kPfStages) - 1) & 1);
+        if (t >= kPfStages) ok = mbar_wait(empty0 + 8 * st, ((t / kPfStages) - 1) & 1);
         if (!ok) {
           if (lane == 0) atomicOr(p.err, kErrTimeout);
           break;
         }
         const int b0 = t * bpt;
         const int nb = min(bpt, nblk - b0);
-        const uint32_t full = kv_full0 + 8 * st;
+        const uint32_t full = full0 + 8 * st;
         if (lane == 0) mbar_arrive_expect_tx(full, tx_block * nb);
         __syncwarp();
         if (lane < nb) {  // one block per lane, issued together
           const int phys = __ldg(bt_row + b0 + lane);
-          if (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks) atomicOr(p.err, kErrBlockId);
-          const uint32_t kdst = base + kKVOff + st * 2 * kTileBytes + lane * p.bs * 128;
-          const uint32_t vdst = kdst + kTileBytes;
-          tma_load_4d(kdst, &tmK, full, 0, 0, hkv, phys);
-          tma_load_4d(kdst + kSegBytes, &tmK, full, 64, 0, hkv, phys);
-          tma_load_4d(vdst, &tmV, full, 0, 0, hkv, phys);
-          tma_load_4d(vdst + kSegBytes, &tmV, full, 64, 0, hkv, phys);
+          if (is_k && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
+          const uint32_t dst = dst0 + st * 2 * kTileBytes + lane * p.bs * 128;
+          tma_load_4d(dst, map, full, 0, 0, hkv, phys);
+          tma_load_4d(dst + kSegBytes, map, full, 64, 0, hkv, phys);
         }
         __syncwarp();
       }
@@ -155,30 +170,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint32_t id_qk = tc_idesc_f16(p.bf16 != 0, false, kPfRows, kPfTile);
       const uint32_t id_pv = tc_idesc_f16(p.bf16 != 0, true, kPfRows, 128);
       bool ok = mbar_wait(q_full, 0);
-      for (int t = 0; ok && t < ntiles; ++t) {
+      // S(t) = Q K(t)^T into S buffer t % 2, both operands K-major (channels
+      // contiguous), 16 channels per step
+      auto issue_qk = [&](int t) -> bool {
         const int st = t % kPfStages;
-        if (!(ok = mbar_wait(kv_full0 + 8 * st, (t / kPfStages) & 1))) break;
+        if (!mbar_wait(k_full0 + 8 * st, (t / kPfStages) & 1)) return false;
         tc_fence_after();
-        const uint32_t k_s = base + kKVOff + st * 2 * kTileBytes, v_s = k_s + kTileBytes;
-        // S = Q K^T: both operands K-major (channels contiguous), 16 channels per step
+        const uint32_t k_s = base + kKVOff + st * 2 * kTileBytes;
+        const uint32_t tS = tS0 + (t & 1) * 128;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t off = (j >> 2) * kSegBytes + (j & 3) * 32;
           tc_mma_f16(tS, tc_desc_sw128(q_s + off, 16, 1024), tc_desc_sw128(k_s + off, 16, 1024), id_qk, j > 0);
         }
-        tc_commit(s_full);
-        if (!(ok = mbar_wait(p_full, t & 1))) break;
+        tc_commit(s_full0 + 8 * (t & 1));
+        tc_commit(k_empty0 + 8 * st);
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        // the next tile's scores overlap this tile's softmax; its S buffer was
+        // released when the softmax of tile t - 1 arrived on p_full
+        if (t + 1 < ntiles && !(ok = issue_qk(t + 1))) break;
+        if (!(ok = mbar_wait(p_full0 + 8 * (t & 1), (t >> 1) & 1))) break;
+        const int st = t % kPfStages;
+        if (!(ok = mbar_wait(v_full0 + 8 * st, (t / kPfStages) & 1))) break;
         tc_fence_after();
         // O += P V: P K-major (tokens contiguous); V channel-major: 64-channel
         // halves 16 KB apart, 8-token groups 1 KB apart, 16 tokens per step
+        const uint32_t v_s = base + kKVOff + st * 2 * kTileBytes + kTileBytes;
+        const uint32_t p_s = p_s0 + (t & 1) * kTileBytes;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint64_t a = tc_desc_sw128(p_s + (j >> 2) * kSegBytes + (j & 3) * 32, 16, 1024);
           const uint64_t b = tc_desc_sw128(v_s + j * 2048, kSegBytes, 1024);
           tc_mma_f16(tO, a, b, id_pv, (t > 0 || j > 0) ? 1u : 0u);
         }
-        tc_commit(o_done);
-        tc_commit(kv_empty0 + 8 * st);
+        tc_commit(o_done0 + 8 * (t & 1));
+        tc_commit(v_empty0 + 8 * st);
       }
       if (!ok) atomicOr(p.err, kErrTimeout);
     }
@@ -187,39 +216,55 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = tid;                 // query row = TMEM lane
     const int pos = pos0 + r;          // its position; it attends to tokens 0..pos
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    float m = -CUDART_INF_F, l = 0.f;
+    float m = -CUDART_INF_F, l = 0.f;  // m: this row's reference max (base 2)
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int st = t % kPfStages;
-      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full, t & 1)))) break;
+      const int buf = t & 1;
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full0 + 8 * buf, (t >> 1) & 1)))) break;
       tc_fence_after();
       float sv[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tS0 + buf * 128 + lane_off + c * 32, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
       tmem_wait_ld();
       const int tok0 = t * kPfTile;
-      float mx = -CUDART_INF_F;
+      // 8 independent max / sum chains: one softmax warp per SM sub-partition
+      // has nothing else to hide the latency of long dependent chains with
+      float mx8[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx8[a] = -CUDART_INF_F;
+      const int lim = pos - tok0;  // last visible column of this tile
 #pragma unroll
       for (int k = 0; k < 128; ++k) {
-        const float x = (tok0 + k <= pos) ? sv[k] * p.scale_log2 : -CUDART_INF_F;
+        const float x = (k <= lim) ? sv[k] * p.scale_log2 : -CUDART_INF_F;
         sv[k] = x;
-        mx = fmaxf(mx, x);
+        mx8[k & 7] = fmaxf(mx8[k & 7], x);
       }
-      const float m_new = fmaxf(m, mx);
-      const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-      float alpha = ex2(m - m_use);
-      float sum = 0.f;
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // the reference max moves only when this tile exceeds it by more than
+      // the threshold; O and l are then scaled by alpha = 2^(m_old - m_new)
+      const bool bump = mx > m + kRescaleThreshold;  // false while both are -inf
+      float alpha = 1.f;
+      if (bump) {
+        alpha = m == -CUDART_INF_F ? 0.f : ex2(m - mx);
+        m = mx;
+      }
+      const float m_use = m == -CUDART_INF_F ? 0.f : m;
+      float sum8[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
 #pragma unroll
       for (int k = 0; k < 128; ++k) {
         sv[k] = ex2(sv[k] - m_use);
-        sum += sv[k];
+        sum8[k & 7] += sv[k];
       }
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + sum;
-      m = m_new;
-      // P.V of the previous tile must be done before P and O are touched again
-      if (t > 0 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(o_done, (t - 1) & 1)))) break;
-      tc_fence_after();
-      uint8_t* prow = smem + kPOff + r * 128;
+      // P buffer `buf` was last read by P.V of tile t - 2
+      if (t >= 2 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(o_done0 + 8 * buf, ((t >> 1) - 1) & 1)))) break;
+      uint8_t* prow = smem + kPOff + buf * kTileBytes + r * 128;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         uint4 w;
@@ -230,19 +275,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint32_t off = swz128(static_cast<uint32_t>(r * 128 + (c & 7) * 16)) - r * 128;
         *reinterpret_cast<uint4*>(prow + (c >> 3) * kSegBytes + off) = w;
       }
-      if (t == ntiles - 1 && r >= kv_len - tok0) {
+      if (t == ntiles - 1) {
         // rows of the last V tile past the context hold whatever the pool had:
-        // zero them so that 0 * value cannot produce NaN in P.V
-        uint8_t* vrow = smem + kKVOff + st * 2 * kTileBytes + kTileBytes + r * 128;
+        // once V has landed, zero them so that 0 * value cannot make NaN in P.V
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(v_full0 + 8 * st, (t / kPfStages) & 1)))) break;
+        if (r >= kv_len - tok0) {
+          uint8_t* vrow = smem + kKVOff + st * 2 * kTileBytes + kTileBytes + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vrow + kSegBytes + c * 16) = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + kSegBytes + c * 16) = make_uint4(0, 0, 0, 0);
+          }
         }
       }
-      // rescale this row of O when the running max moved (warp-uniform: the
-      // TMEM moves are warp-wide; rows whose max did not move multiply by 1)
-      if (t > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+      // rescale O rows whose reference moved, once P.V of tile t - 1 is done
+      // (warp-uniform: the TMEM moves are warp-wide; other rows multiply by 1)
+      if (t > 0 && __any_sync(0xFFFFFFFFu, bump)) {
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(o_done0 + 8 * (buf ^ 1), ((t - 1) >> 1) & 1)))) break;
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
@@ -256,9 +306,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full0 + 8 * buf);
     }
-    if (ok && ntiles > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(o_done, (ntiles - 1) & 1));
+    if (ok && ntiles > 0)
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(o_done0 + 8 * ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1));
     if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
