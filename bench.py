@@ -201,7 +201,8 @@ def recorded_traffic(workload: str, kernel: str):
     for ln in text.splitlines():
         if ":" in ln:
             k, v = ln.split(":", 1)
-            vals[k.strip()] = v.strip()
+            v = v.split()
+            vals[k.strip()] = v[0] if v else ""
     if vals.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
