@@ -149,7 +149,8 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * 128 query tokens) streams 128-token K/V tiles through the block table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, 128] of q_dtype
  * Supported: head_dim 128, 16-bit caches of the q dtype, block size 8, 16 or
- * 32.  Other arguments as pa_decode (no kv_scale: 16-bit caches only).
+ * 32, scale > 0.  Other arguments as pa_decode (no kv_scale: 16-bit caches
+ * only).
  */
 PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                       int32_t num_q_heads, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,

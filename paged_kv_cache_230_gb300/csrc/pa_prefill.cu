@@ -229,20 +229,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld32(tS0 + buf * 128 + lane_off + c * 32, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
       tmem_wait_ld();
       const int tok0 = t * kPfTile;
-      // 8 independent max / sum chains: one softmax warp per SM sub-partition
-      // has nothing else to hide the latency of long dependent chains with
+      const int lim = pos - tok0;  // last visible column of this tile
+      // the causal mask only matters on tiles that reach past some row's
+      // position (warp-uniform test); elsewhere every column is visible
+      if (!__all_sync(0xFFFFFFFFu, lim >= kPfTile - 1)) {
+#pragma unroll
+        for (int k = 0; k < 128; ++k) sv[k] = (k <= lim) ? sv[k] : -CUDART_INF_F;
+      }
+      // max of the raw scores (the scale is positive), 8 independent chains:
+      // one softmax warp per SM sub-partition has nothing else to hide the
+      // latency of long dependent chains with
       float mx8[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) mx8[a] = -CUDART_INF_F;
-      const int lim = pos - tok0;  // last visible column of this tile
 #pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        const float x = (k <= lim) ? sv[k] * p.scale_log2 : -CUDART_INF_F;
-        sv[k] = x;
-        mx8[k & 7] = fmaxf(mx8[k & 7], x);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int k = 0; k < 128; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+      const float mx = p.scale_log2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                            fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // the reference max moves only when this tile exceeds it by more than
       // the threshold; O and l are then scaled by alpha = 2^(m_old - m_new)
       const bool bump = mx > m + kRescaleThreshold;  // false while both are -inf
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
 #pragma unroll
       for (int k = 0; k < 128; ++k) {
-        sv[k] = ex2(sv[k] - m_use);
+        sv[k] = ex2(fmaf(sv[k], p.scale_log2, -m_use));  // 2^(scale log2e s - m)
         sum8[k & 7] += sv[k];
       }
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
