@@ -456,6 +456,13 @@ def run_blocks(args, local):
         torch.cuda.synchronize()
         us = 1e3 * e0.elapsed_time(e1) / K
         res[name] = {"us": us, "gbs": 2 * moved / (us * 1e-6) / 1e9}
+    # KV fragmentation of the host block manager on the gqa8b length mix:
+    # unused tail slots over all slots of the blocks the sequences hold
+    lens = W.config_lengths(2, 2)
+    bm = pa.BlockManager(int(sum(-(-int(x) // bs) for x in lens)), bs)
+    for sid, x in enumerate(lens):
+        bm.add_sequence(sid, int(x))
+    res["fragmentation_gqa8b"] = bm.tail_waste() / ((bm.num_blocks - bm.num_free_blocks()) * bs)
     peak, kind = measured_hbm_peak()
     line = {"metric": "block copy GB/s (read + write)", "value": res["copy_blocks"]["gbs"], "unit": "GB/s",
             "n_gpus": 1, "steps": min(args.steps, 200), "warmup": args.warmup, "higher_is_better": True,

@@ -17,10 +17,11 @@
 //           channels, K = 128 tokens, V read channel-major) into a third;
 //   warps 0-3  one thread per query row (= TMEM lane): reads its S row with
 //           tcgen05.ld, applies the causal mask and the online softmax in
-//           base 2 (no cross-thread reduction), writes P as 16-bit values to
-//           shared memory in the A-operand layout (two buffers), rescales its
-//           O row in TMEM when its reference max moved by more than 2^8, and
-//           at the end writes O / l.
+//           base 2 (no cross-thread reduction), writes P as 16-bit pairs
+//           over the first 64 columns of its own S buffer in TMEM (the A
+//           operand of P.V comes from TMEM, so shared memory only feeds K, V
+//           and Q to the tensor core), rescales its O row in TMEM when its
+//           reference max moved by more than 2^8, and at the end writes O / l.
 // Every mbarrier wait gives up after about one second (error bit set).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,9 +43,11 @@ constexpr int kSegBytes = kPfTile * 128;  // 64 channels (128 B) of 128 rows
 constexpr int kTileBytes = 2 * kSegBytes;  // 128 rows x 128 channels x 2 B
 constexpr int kQOff = 0;
 constexpr int kKVOff = kQOff + kTileBytes;                    // stage st: K at +2*st*tile, V after it
-constexpr int kPOff = kKVOff + kPfStages * 2 * kTileBytes;   // 2 buffers of P, A operand of P.V
-constexpr int kBarOff = kPOff + 2 * kTileBytes;
-constexpr int kSmemBytes = 1024 + kBarOff + 128;  // 15 mbarriers + TMEM address slot
+constexpr int kBarOff = kKVOff + kPfStages * 2 * kTileBytes;
+// mbarriers: q, K full/empty and V full/empty per stage, S full, P full and
+// O done per TMEM buffer; then the TMEM address slot
+constexpr int kBarBytes = 8 + 32 * kPfStages + 48 + 8;
+constexpr int kSmemBytes = 1024 + kBarOff + kBarBytes;
 constexpr uint32_t kTmemCols = 512;  // S buffers in columns [0, 128) and [128, 256), O in [256, 384)
 // A row's reference max moves only when the tile max exceeds it by more than
 // this (base 2): probabilities then stay below 2^8 and O is rescaled rarely.
@@ -52,7 +55,35 @@ constexpr float kRescaleThreshold = 8.f;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ ((off >> 3) & 0x70); }
+// Paired fp32 arithmetic: two lanes of one 64-bit register per FMA/ADD issue,
+// and a three-input max, halve the instruction count of the row softmax.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t pack16(float a, float b, int bf16) {
   if (bf16) {
@@ -70,14 +101,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t base = smem_u32(smem);
-  const uint32_t q_s = base + kQOff, p_s0 = base + kPOff;
+  const uint32_t q_s = base + kQOff;
   const uint32_t bar0 = base + kBarOff;
   // per-buffer barriers (index = tile parity), so no wait is on an ambiguous
   // phase; K and V have their own buffers: K of a tile is released as soon as
   // its QK^T completes, V only after its P.V
-  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40, v_empty0 = bar0 + 56;
-  const uint32_t s_full0 = bar0 + 72, p_full0 = bar0 + 88, o_done0 = bar0 + 104;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
+  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = k_full0 + 8 * kPfStages;
+  const uint32_t v_full0 = k_empty0 + 8 * kPfStages, v_empty0 = v_full0 + 8 * kPfStages;
+  const uint32_t s_full0 = v_empty0 + 8 * kPfStages, p_full0 = s_full0 + 16, o_done0 = p_full0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kBarBytes - 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqt = (p.C + kPfRows - 1) / kPfRows;
@@ -196,15 +228,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int st = t % kPfStages;
         if (!(ok = mbar_wait(v_full0 + 8 * st, (t / kPfStages) & 1))) break;
         tc_fence_after();
-        // O += P V: P K-major (tokens contiguous); V channel-major: 64-channel
-        // halves 16 KB apart, 8-token groups 1 KB apart, 16 tokens per step
+        // O += P V: P from TMEM (16 tokens = 8 columns per step); V
+        // channel-major: 64-channel halves 16 KB apart, 8-token groups 1 KB apart
         const uint32_t v_s = base + kKVOff + st * 2 * kTileBytes + kTileBytes;
-        const uint32_t p_s = p_s0 + (t & 1) * kTileBytes;
+        const uint32_t p_t = tS0 + (t & 1) * 128;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint64_t a = tc_desc_sw128(p_s + (j >> 2) * kSegBytes + (j & 3) * 32, 16, 1024);
           const uint64_t b = tc_desc_sw128(v_s + j * 2048, kSegBytes, 1024);
-          tc_mma_f16(tO, a, b, id_pv, (t > 0 || j > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tO, p_t + j * 8, b, id_pv, (t > 0 || j > 0) ? 1u : 0u);
         }
         tc_commit(o_done0 + 8 * (t & 1));
         tc_commit(v_empty0 + 8 * st);
@@ -243,7 +274,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int a = 0; a < 8; ++a) mx8[a] = -CUDART_INF_F;
 #pragma unroll
-      for (int k = 0; k < 128; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+      for (int k = 0; k < 128; k += 2) mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], sv[k], sv[k + 1]);
       const float mx = p.scale_log2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // the reference max moves only when this tile exceeds it by more than
@@ -255,28 +286,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         m = mx;
       }
       const float m_use = m == -CUDART_INF_F ? 0.f : m;
+      // p = 2^(scale log2e s - m) two columns per FMA, row sum in 4 paired chains
+      const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_use, -m_use);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (+0, +0) pairs
+#pragma unroll
+      for (int k = 0; k < 128; k += 2) {
+        float lo, hi;
+        f2unpack(ffma2(f2pack(sv[k], sv[k + 1]), sc2, nm2), lo, hi);
+        sv[k] = ex2(lo);
+        sv[k + 1] = ex2(hi);
+        acc[(k >> 1) & 3] = fadd2(acc[(k >> 1) & 3], f2pack(sv[k], sv[k + 1]));
+      }
       float sum8[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        sv[k] = ex2(fmaf(sv[k], p.scale_log2, -m_use));  // 2^(scale log2e s - m)
-        sum8[k & 7] += sv[k];
-      }
+      for (int a = 0; a < 4; ++a) f2unpack(acc[a], sum8[2 * a], sum8[2 * a + 1]);
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + sum;
-      // P buffer `buf` was last read by P.V of tile t - 2
-      if (t >= 2 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(o_done0 + 8 * buf, ((t >> 1) - 1) & 1)))) break;
-      uint8_t* prow = smem + kPOff + buf * kTileBytes + r * 128;
+      // P(t) over the first 64 columns of S buffer `buf`: S(t) was issued
+      // after P.V of tile t - 2, so that MMA has finished reading P(t - 2)
+      {
+        uint32_t pw[64];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint4 w;
-        w.x = pack16(sv[8 * c + 0], sv[8 * c + 1], p.bf16);
-        w.y = pack16(sv[8 * c + 2], sv[8 * c + 3], p.bf16);
-        w.z = pack16(sv[8 * c + 4], sv[8 * c + 5], p.bf16);
-        w.w = pack16(sv[8 * c + 6], sv[8 * c + 7], p.bf16);
-        const uint32_t off = swz128(static_cast<uint32_t>(r * 128 + (c & 7) * 16)) - r * 128;
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * kSegBytes + off) = w;
+        for (int c = 0; c < 64; ++c) pw[c] = pack16(sv[2 * c], sv[2 * c + 1], p.bf16);
+        tmem_st32(tS0 + buf * 128 + lane_off, pw);
+        tmem_st32(tS0 + buf * 128 + lane_off + 32, pw + 32);
       }
       if (t == ntiles - 1) {
         // rows of the last V tile past the context hold whatever the pool had:
@@ -305,8 +338,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int k = 0; k < 32; ++k) o[k] *= alpha;
           tmem_st32(tO + lane_off + c * 32, o);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full0 + 8 * buf);

@@ -152,3 +152,41 @@ def test_oracle_block_moves_match_numpy_indexing():
     assert oracle.scatter_blocks(kz, vz, buf, ids) == 0
     assert np.array_equal(kz[ids], kc[ids]) and np.array_equal(vz[ids], vc[ids])
     assert oracle.copy_blocks(kc, vc, np.array([[11, 0]])) == 1
+
+
+def fragmentation(bm, ids):
+    """Unused slots at the ends of the sequences' last blocks over all slots of
+    the blocks the sequences hold (shared blocks counted once)."""
+    held = set()
+    for s in ids:
+        held.update(bm.block_table(s)[0])
+    return bm.tail_waste() / (len(held) * bm.block_size)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_fragmentation_on_the_workload_length_mixes_is_below_four_percent(idx):
+    """Paging allocates per token: the review (§3 Q3, §9 "Memory Management",
+    §10 table) puts the waste below 4 %, and §11 bounds it by block_size - 1
+    slots per sequence.  Checked on each decode workload's length mix, with the
+    shared-prefix mix built by forking prompts and appending private tails."""
+    from paged_kv_cache_230_gb300 import workloads as W
+    L = W.config_lengths(idx, idx)
+    bs = 16
+    bm = pa.BlockManager(int(sum(-(-int(n) // bs) for n in L)) + 64, bs)
+    if idx == 4:
+        for p in range(8):
+            bm.add_sequence(10_000 + p, 2048)
+        for s, n in enumerate(L):
+            bm.fork(10_000 + s % 8, s)
+            bm.append_tokens(s, int(n) - 2048)
+        for p in range(8):
+            bm.free_sequence(10_000 + p)
+    else:
+        for s, n in enumerate(L):
+            bm.add_sequence(s, int(n))
+    ids = list(range(len(L)))
+    for s in ids:
+        tb, n = bm.block_table(s)
+        assert n == L[s] and len(tb) * bs - n <= bs - 1
+    assert bm.check() == 0
+    assert fragmentation(bm, ids) < 0.04
