@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
     ap.add_argument("--qlen", type=int, default=1, help="new query tokens per sequence (multi-token decode)")
+    ap.add_argument("--block-size", type=int, default=16, help="KV block size of the prefill workload (8, 16, 32)")
     ap.add_argument("--op", default="decode", choices=["decode", "blocks", "prefill"],
                     help="blocks: time copy-on-write block copies and swap-out/in through pinned host memory")
     ap.add_argument("--ref-budget", type=float, default=0.0,
@@ -141,7 +142,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, watts = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -152,13 +153,17 @@ class ClockSampler:
                 mx = float(f[1])
             except ValueError:
                 continue
+            try:
+                watts.append(float(f[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w": statistics.median(watts) if watts else None}
 
 
 # --------------------------------------------------------------------------
@@ -441,6 +446,10 @@ def run_blocks(args, local):
     block = Hkv * bs * D * 2
     moved = 2 * n * block  # K and V blocks per call
     res = {}
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     for name, fn in (("copy_blocks", lambda: pa.copy_blocks(kc, vc, pairs)),
                      ("gather_to_host", lambda: pa.gather_blocks(host, kc, vc, ids)),
                      ("scatter_from_host", lambda: pa.scatter_blocks(kc, vc, host, ids))):
@@ -456,6 +465,7 @@ def run_blocks(args, local):
         torch.cuda.synchronize()
         us = 1e3 * e0.elapsed_time(e1) / K
         res[name] = {"us": us, "gbs": 2 * moved / (us * 1e-6) / 1e9}
+    clocks = sampler.stop() if sampler else None
     # KV fragmentation of the host block manager on the gqa8b length mix:
     # unused tail slots over all slots of the blocks the sequences hold
     lens = W.config_lengths(2, 2)
@@ -468,7 +478,7 @@ def run_blocks(args, local):
             "n_gpus": 1, "steps": min(args.steps, 200), "warmup": args.warmup, "higher_is_better": True,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "blocks_gqa8b_pool", "blocks_per_call": n, "block_bytes_per_cache": block},
-            "ops": res,
+            "ops": res, "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": res["copy_blocks"]["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": res["copy_blocks"]["gbs"] / peak, "peak_source": kind, "kernel": "pa_copy_blocks"}}
     print(json.dumps(line), flush=True)
@@ -498,7 +508,8 @@ def run_prefill(args, local):
     S = args.seqs if args.seqs > 0 else 16
     C = args.qlen if args.qlen > 1 else 2048
     L = 2 * C
-    wl = W.make_workload(name="prefill_gqa8b", seed=7, context_lens=[L] * S, Hq=32, Hkv=8, D=128, bs=16,
+    bs = getattr(args, "block_size", 16)
+    wl = W.make_workload(name="prefill_gqa8b", seed=7, context_lens=[L] * S, Hq=32, Hkv=8, D=128, bs=bs,
                          q_dtype="bf16", kv_dtype="bf16", qlen=C)
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
@@ -510,21 +521,35 @@ def run_prefill(args, local):
     for _ in range(max(3, args.warmup)):
         run()
     torch.cuda.synchronize()
-    K = max(1, min(args.steps, 100))
+    # time enough launches to fill about two seconds, so that the clock
+    # sampler (100 ms period) sees the kernel under load
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    est_ms = max(1e-3, e0.elapsed_time(e1) / 3)
+    K = max(1, args.steps, min(20000, int(2000.0 / est_ms)))
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(K):
         run()
     e1.record()
     torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
     us = 1e3 * e0.elapsed_time(e1) / K
     tflops = flops / (us * 1e-6) / 1e12
     peak, kind = measured_tensor_peak()
     line = {"metric": "paged prefill attention TFLOP/s (causal FLOPs)", "value": tflops, "unit": "TFLOP/s",
             "n_gpus": 1, "steps": K, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": wl.name, "num_seqs": S, "chunk": C, "context": L,
-                                            "q_heads": 32, "kv_heads": 8, "head_dim": 128},
-            "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6),
+                                            "q_heads": 32, "kv_heads": 8, "head_dim": 128, "block_size": bs},
+            "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6), "clocks": clocks,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "peak_source": kind, "kernel": "pa_prefill"}}
     print(json.dumps(line), flush=True)
