@@ -200,7 +200,7 @@ cudaError_t launch_decode(const pa::DecodeParams& p, const CUtensorMap& tk, cons
 // Pmax partitions, so launch and pipeline ramp costs are paid per run, not
 // per partition.
 #ifndef PA_SPLIT_CTAS_PER_SLOT
-#define PA_SPLIT_CTAS_PER_SLOT 8
+#define PA_SPLIT_CTAS_PER_SLOT 16
 #endif
 int parts_per_cta(int S, int Hkv, int Pmax) {
   static int sms[kMaxDevices] = {0};

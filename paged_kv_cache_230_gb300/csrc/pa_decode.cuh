@@ -59,9 +59,6 @@ struct Geom {
   static constexpr int SEG_BYTES = kTileTokens * BOXB;
   static constexpr int HALF_BYTES = NSEG * SEG_BYTES;       // K (or V) bytes per stage
   static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
-  static constexpr int NST_RAW = kRingBytes / STAGE_BYTES;
-  static constexpr int NST = NST_RAW < 2 ? 2 : (NST_RAW > 8 ? 8 : NST_RAW);
-  static constexpr int RING = NST * STAGE_BYTES;
   static_assert(SEG_BYTES % 1024 == 0, "segments must keep the swizzle atom alignment");
 };
 
@@ -72,14 +69,14 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
   return off ^ ((off >> 3) & Gm::SWZ);
 }
 
+// Dynamic shared memory of one CTA: alignment slack, the ring of `nst`
+// stages, the [NG][D] output area (q staging at start-up), the ring's
+// mbarriers, the warps' (m, l), the run's (m, l) and, in the split variant
+// only, the run accumulator [NG][D] (last, so one-pass launches omit it).
 template <int NG, int D>
-__host__ __device__ constexpr int decode_smem_bytes_for(int ring, int nst) {
-  return 1024 + ring + 2 * NG * D * 4 + 2 * nst * 8 + kConsumerWarps * NG * 2 * 4 + 2 * NG * 2 * 4;
-}
-
-template <int KV, int D, int NG>
-constexpr int decode_smem_bytes() {
-  return decode_smem_bytes_for<NG, D>(Geom<KV, D>::RING, Geom<KV, D>::NST);
+__host__ __device__ constexpr int decode_smem_bytes_for(int ring, int nst, bool split) {
+  return 1024 + ring + NG * D * 4 + 2 * nst * 8 + kConsumerWarps * NG * 2 * 4 + 2 * NG * 2 * 4 +
+         (split ? NG * D * 4 : 0);
 }
 
 __device__ __forceinline__ float load_q(const void* q, int64_t idx, int q_dtype) {
@@ -368,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   using Gm = Geom<KV, D>;
-  constexpr int NST = Gm::NST;
+  const int NST = p.nst;  // ring stages, chosen per launch from the shared-memory budget
+  const int RING = NST * Gm::STAGE_BYTES;
   constexpr int NCW = kConsumerWarps;
   constexpr int TILE = kTileTokens;
 
@@ -377,12 +375,13 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
   const uint32_t ring_u32 = smem_u32(smem);
   // q staging at start-up, then the epilogue's output area: [NG][D] floats
-  float* qbuf = reinterpret_cast<float*>(smem + Gm::RING);
+  float* qbuf = reinterpret_cast<float*>(smem + RING);
   float* area = qbuf;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::RING + NG * D * 4);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING + NG * D * 4);
   float* ml = reinterpret_cast<float*>(bars + 2 * NST);  // [NCW][NG][2]
   float* cml = ml + NCW * NG * 2;                         // [2][NG][2] run (m, l), double-buffered
-  float* carea = reinterpret_cast<float*>(smem + Gm::RING + NG * D * 4 + 2 * NST * 8 + (NCW + 2) * NG * 2 * 4);
+  // [NG][D] run accumulator: split variant only (not allocated otherwise)
+  float* carea = reinterpret_cast<float*>(smem + RING + NG * D * 4 + 2 * NST * 8 + (NCW + 2) * NG * 2 * 4);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + NST * 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -940,14 +939,31 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodePa
   }
 }
 
+// Ring stages: as many as fit when the variant's CTAs per SM (its register
+// budget) share the SM's shared memory, between 2 and 8.  More stages keep
+// more loads in flight per SM, which the two-CTA variants need to stay near
+// the HBM rate.
 template <int KV, int D, bool USE_MMA, int NG>
-cudaError_t launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+int ring_stages(bool split) {
+  constexpr int kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
+  constexpr int ctas = decode_min_ctas<D, USE_MMA, NG>();
+  const int budget = kSmemPerSm / ctas - kReservedPerCta;
+  const int fixed = decode_smem_bytes_for<NG, D>(0, 0, split);
+  int nst = (budget - fixed) / (Geom<KV, D>::STAGE_BYTES + 16);
+  return nst < 2 ? 2 : (nst > 8 ? 8 : nst);
+}
+
+template <int KV, int D, bool USE_MMA, int NG>
+cudaError_t launch_one(const DecodeParams& p0, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        cudaStream_t st) {
-  constexpr int smem = decode_smem_bytes<KV, D, NG>();
+  DecodeParams p = p0;
+  const bool split = p.partition_size > 0;
+  p.nst = ring_stages<KV, D, USE_MMA, NG>(split);
+  const int smem = decode_smem_bytes_for<NG, D>(p.nst * Geom<KV, D>::STAGE_BYTES, p.nst, split);
   auto kern = decode_kernel<KV, D, USE_MMA, NG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int nchunk = p.partition_size > 0 ? (p.Pmax + p.parts_per_cta - 1) / p.parts_per_cta : 1;
+  const int nchunk = split ? (p.Pmax + p.parts_per_cta - 1) / p.parts_per_cta : 1;
   const long long grid = static_cast<long long>(p.S) * p.Hkv * nchunk;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmK, tmV, p);
   return cudaGetLastError();

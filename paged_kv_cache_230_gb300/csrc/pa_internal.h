@@ -12,16 +12,12 @@ namespace pa {
 #ifndef PA_CONSUMER_WARPS
 #define PA_CONSUMER_WARPS 4
 #endif
-#ifndef PA_RING_KB
-#define PA_RING_KB 64
-#endif
 #ifndef PA_MIN_CTAS_PER_SM
 #define PA_MIN_CTAS_PER_SM 3
 #endif
 constexpr int kConsumerWarps = PA_CONSUMER_WARPS;    // warps that compute
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kTileTokens = 16 * kConsumerWarps;     // tokens per pipeline stage
-constexpr int kRingBytes = PA_RING_KB * 1024;        // target bytes of the K/V stage ring
 constexpr int kMinCtasPerSm = PA_MIN_CTAS_PER_SM;
 constexpr int kMaxGroup = 16;                     // largest query group G
 
@@ -42,6 +38,7 @@ struct DecodeParams {
   int partition_size;         // tokens per partition; 0 = whole context per CTA
   int Pmax;                   // partitions per sequence (1 without split)
   int parts_per_cta;          // split: consecutive partitions streamed by one CTA
+  int nst;                    // ring stages (set by the launcher)
   float scale_log2;           // scale * log2(e)
   float kv_scale;             // FP8 dequantisation scale (1 for 16-bit caches)
 };
