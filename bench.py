@@ -343,7 +343,7 @@ def run_ours(args, wl, world, rank, local, pg):
     dec_avg = sum(dec_ms) / K
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
-    kernel_name = "decode_multi" if wl.qlen > 1 else ("decode_split" if P else "decode")
+    kernel_name = ("decode_multi_split" if P else "decode_multi") if wl.qlen > 1 else ("decode_split" if P else "decode")
     traffic = recorded_traffic(wl.name, kernel_name)
 
     e2e = None
@@ -530,7 +530,7 @@ def run_prefill(args, local):
     e1.record()
     torch.cuda.synchronize()
     est_ms = max(1e-3, e0.elapsed_time(e1) / 3)
-    K = max(1, args.steps, min(20000, int(2000.0 / est_ms)))
+    K = max(1, args.steps) if args.no_clocks else max(1, args.steps, min(20000, int(2000.0 / est_ms)))
     sampler = ClockSampler(local) if not args.no_clocks else None
     if sampler:
         sampler.start()

@@ -188,6 +188,31 @@ PA_API int pa_decode_split(void *out, const void *q, int32_t q_dtype, int32_t nu
                     size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Workspace bytes pa_decode_multi_split needs: num_seqs * num_q_tokens *
+ * num_q_heads * ceil(max_context_len / partition_size) * (head_dim + 2) * 4.
+ * Returns 0 for invalid sizes.
+ */
+PA_API size_t pa_decode_multi_split_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                                                   int32_t head_dim, int32_t max_context_len,
+                                                   int32_t partition_size);
+
+/*
+ * pa_decode_multi_split: pa_decode_multi (num_q_tokens new tokens per
+ * sequence, causal among them) computed per partition of partition_size
+ * tokens and merged by log-sum-exp as in pa_decode_split.  Long contexts are
+ * spread over several CTAs, so one long sequence no longer sets the time of
+ * the whole batch.  A partition that lies wholly after a new token's position
+ * contributes nothing to that token.  Arguments as pa_decode_multi plus
+ * max_context_len, partition_size and the workspace as pa_decode_split.
+ */
+PA_API int pa_decode_multi_split(void *out, const void *q, int32_t q_dtype, int32_t num_seqs,
+                                 int32_t num_q_tokens, int32_t num_q_heads, const void *k_cache,
+                                 const void *v_cache, const pa_cache_desc *cache, const int32_t *block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t *context_lens, float scale,
+                                 float kv_scale, int32_t max_context_len, int32_t partition_size,
+                                 void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_split_noalloc: pa_decode_split without a workspace argument, for
  * callers that cannot allocate device memory when they call (for example a
  * serving process whose KV-cache pool already holds nearly all of HBM, or a

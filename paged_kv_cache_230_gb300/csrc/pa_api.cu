@@ -351,12 +351,60 @@ int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int3
   return finish(pa::launch_prefill(p, tq, tk, tv, st), st);
 }
 
+size_t pa_decode_multi_split_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                                            int32_t head_dim, int32_t max_context_len, int32_t partition_size) {
+  if (num_seqs < 0 || num_q_tokens < 1 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+      partition_size <= 0)
+    return 0;
+  const int64_t np = split_partitions(max_context_len, partition_size);
+  return static_cast<size_t>(num_seqs) * num_q_tokens * num_q_heads * np * (head_dim + 2) * sizeof(float);
+}
+
 size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                       int32_t max_context_len, int32_t partition_size) {
-  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size <= 0) return 0;
-  const int64_t np = split_partitions(max_context_len, partition_size);
-  return static_cast<size_t>(num_seqs) * num_q_heads * np * (head_dim + 2) * sizeof(float);
+  return pa_decode_multi_split_workspace_size(num_seqs, 1, num_q_heads, head_dim, max_context_len, partition_size);
 }
+
+}  // extern "C"
+
+namespace {
+
+// Split decode of one or several new tokens per sequence: the partition
+// kernel, then the log-sum-exp merge of the runs, on one stream.
+int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition_size, void* workspace,
+                      size_t workspace_bytes, pa_stream_t stream) {
+  int rc = check_decode(a);
+  if (rc) return rc;
+  if (partition_size <= 0 || partition_size % pa::kTileTokens || max_context_len < 0) return PA_ERR_INVALID_ARG;
+  if (a.num_seqs == 0) return PA_OK;
+  const pa_cache_desc* cache = a.cache;
+  const int64_t np = split_partitions(max_context_len, partition_size);
+  if (static_cast<int64_t>(a.num_seqs) * cache->num_kv_heads * np > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a.num_seqs) * a.qlen * a.num_q_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
+  const size_t need = pa_decode_multi_split_workspace_size(a.num_seqs, a.qlen, a.num_q_heads, cache->head_dim,
+                                                           max_context_len, partition_size);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, a.k_cache, cache)) || (rc = make_cache_tensor_map(&tv, a.v_cache, cache)))
+    return rc;
+  pa::DecodeParams p = make_params(a, err);
+  p.partition_size = partition_size;
+  p.Pmax = static_cast<int>(np);
+  p.parts_per_cta = parts_per_cta(a.num_seqs, cache->num_kv_heads, p.Pmax);
+  const size_t rows = static_cast<size_t>(a.num_seqs) * a.qlen * a.num_q_heads * np;
+  p.ws_ml = static_cast<float*>(workspace);
+  p.ws_o = p.ws_ml + rows * 2;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st);
+  if (e == cudaSuccess) e = pa::launch_lse_merge(p, cache->head_dim, st);
+  return finish(e, st);
+}
+
+}  // namespace
+
+extern "C" {
 
 int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
                     const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
@@ -365,31 +413,17 @@ int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
                     size_t workspace_bytes, pa_stream_t stream) {
   const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, 1, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
-  int rc = check_decode(a);
-  if (rc) return rc;
-  if (partition_size <= 0 || partition_size % pa::kTileTokens || max_context_len < 0) return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0) return PA_OK;
-  const int64_t np = split_partitions(max_context_len, partition_size);
-  if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads * np > INT32_MAX) return PA_ERR_INVALID_ARG;
-  const size_t need = pa_decode_split_workspace_size(num_seqs, num_q_heads, cache->head_dim, max_context_len,
-                                                     partition_size);
-  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-  int* err = device_error_ptr();
-  if (!err) return PA_ERR_CUDA;
-  CUtensorMap tk, tv;
-  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
-    return rc;
-  pa::DecodeParams p = make_params(a, err);
-  p.partition_size = partition_size;
-  p.Pmax = static_cast<int>(np);
-  p.parts_per_cta = parts_per_cta(num_seqs, cache->num_kv_heads, p.Pmax);
-  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * np;
-  p.ws_ml = static_cast<float*>(workspace);
-  p.ws_o = p.ws_ml + rows * 2;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st);
-  if (e == cudaSuccess) e = pa::launch_lse_merge(p, cache->head_dim, st);
-  return finish(e, st);
+  return decode_split_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_multi_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+                          int32_t num_q_heads, const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                          float scale, float kv_scale, int32_t max_context_len, int32_t partition_size,
+                          void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, kv_scale};
+  return decode_split_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream);
 }
 
 // Device address through which kernels may touch `p`: device or managed

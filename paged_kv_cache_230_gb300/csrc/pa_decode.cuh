@@ -453,22 +453,25 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
       const uint32_t full = full0 + 8 * stage;
       if (lane == 0) mbar_arrive_expect_tx(full, tx * nb);
       const uint32_t kdst0 = ring_u32 + stage * Gm::STAGE_BYTES;
-      for (int i = 0; i < nb; ++i) {
-        const int b = b0 + i;
-        if (b >= base + 32) {
-          base += 32;
-          cur = nxt;
-          nxt = (base + 32 + lane < blk_end) ? __ldg(bt_row + base + 32 + lane) : -1;
-        }
-        const int phys = __shfl_sync(0xFFFFFFFFu, cur, b - base);
-        if (lane == 0) {
-          if (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks) atomicOr(p.err, kErrBlockId);
-          const uint32_t kdst = kdst0 + i * bs * Gm::BOXB;
+      // one lane per block of the stage (at most 64 / 8), so the warp issues
+      // every block's tile loads together; issuing them from one lane after
+      // another capped the rate at which a CTA could stream
+      while (b0 >= base + 32) {
+        base += 32;
+        cur = nxt;
+        nxt = (base + 32 + lane < blk_end) ? __ldg(bt_row + base + 32 + lane) : -1;
+      }
+      const int rel = b0 + lane - base;  // table window index, below 64 for lane < nb
+      const int pc = __shfl_sync(0xFFFFFFFFu, cur, rel & 31);
+      const int pn = __shfl_sync(0xFFFFFFFFu, nxt, rel & 31);
+      if (lane < nb) {
+        const int phys = rel < 32 ? pc : pn;
+        if (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks) atomicOr(p.err, kErrBlockId);
+        const uint32_t kdst = kdst0 + lane * bs * Gm::BOXB;
 #pragma unroll
-          for (int sg = 0; sg < Gm::NSEG; ++sg) {
-            tma_load_4d(kdst + sg * Gm::SEG_BYTES, &tmK, full, sg * Gm::BOXE, 0, h, phys);
-            tma_load_4d(kdst + Gm::HALF_BYTES + sg * Gm::SEG_BYTES, &tmV, full, sg * Gm::BOXE, 0, h, phys);
-          }
+        for (int sg = 0; sg < Gm::NSEG; ++sg) {
+          tma_load_4d(kdst + sg * Gm::SEG_BYTES, &tmK, full, sg * Gm::BOXE, 0, h, phys);
+          tma_load_4d(kdst + Gm::HALF_BYTES + sg * Gm::SEG_BYTES, &tmV, full, sg * Gm::BOXE, 0, h, phys);
         }
       }
     }

@@ -51,7 +51,8 @@ class DeviceBatch:
         self.out = torch.empty_like(self.q)
         self.workspace = None
         if self.partition_size:
-            need = pa.decode_split_workspace_size(wl.S, wl.Hq, wl.D, wl.max_context_len, self.partition_size)
+            need = pa.decode_multi_split_workspace_size(wl.S, wl.qlen, wl.Hq, wl.D, wl.max_context_len,
+                                                        self.partition_size)
             self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=d)
 
     def scatter(self) -> None:
@@ -60,7 +61,11 @@ class DeviceBatch:
 
     def decode(self) -> torch.Tensor:
         wl = self.wl
-        if wl.qlen > 1:
+        if wl.qlen > 1 and self.partition_size:
+            pa.decode_multi_split(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                  self.context_lens, wl.scale, wl.kv_scale, wl.max_context_len,
+                                  self.partition_size, self.workspace)
+        elif wl.qlen > 1:
             pa.decode_multi(self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
                             wl.scale, wl.kv_scale)
         elif self.partition_size:

@@ -31,7 +31,8 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: 
           -7: "not enough free blocks", -8: "unknown or duplicate sequence id"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill", "pa_decode_split_workspace_size",
-           "pa_decode_split", "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
+           "pa_decode_split", "pa_decode_multi_split_workspace_size", "pa_decode_multi_split",
+           "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
            "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_num_free_blocks", "pa_bm_refcount",
            "pa_bm_tail_waste", "pa_bm_check", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
@@ -65,6 +66,10 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
     lib.pa_decode_split.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
                                     i32, i32, P, ctypes.c_size_t, P]
+    lib.pa_decode_multi_split_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.pa_decode_multi_split_workspace_size.restype = ctypes.c_size_t
+    lib.pa_decode_multi_split.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32,
+                                          f32, i32, i32, P, ctypes.c_size_t, P]
     lib.pa_decode_split_noalloc.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32,
                                             f32, i32, i32, P]
     D = ctypes.POINTER(CacheDesc)
@@ -96,7 +101,8 @@ def _load() -> ctypes.CDLL:
     lib.pa_set_check_mode.argtypes = [ctypes.c_int]
     lib.pa_get_device_error.argtypes = []
     lib.pa_version.argtypes = []
-    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split", "pa_decode_split_noalloc",
+    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split", "pa_decode_multi_split",
+                 "pa_decode_split_noalloc",
                  "pa_set_check_mode",
                  "pa_get_device_error", "pa_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -268,6 +274,43 @@ def decode_split(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
                                  int(max_context_len), int(partition_size), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(dev))
     _check("pa_decode_split", rc)
+
+
+def decode_multi_split_workspace_size(num_seqs: int, num_q_tokens: int, num_q_heads: int, head_dim: int,
+                                      max_context_len: int, partition_size: int) -> int:
+    return int(lib.pa_decode_multi_split_workspace_size(num_seqs, num_q_tokens, num_q_heads, head_dim,
+                                                        max_context_len, partition_size))
+
+
+def decode_multi_split(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float,
+                       max_context_len: int, partition_size: int = 512,
+                       workspace: Optional[torch.Tensor] = None) -> None:
+    """Multi-token decode (q/out [S, k, Hq, D]) split into partitions merged by
+    log-sum-exp.  ``workspace`` (uint8, at least
+    decode_multi_split_workspace_size bytes) is allocated with torch when not
+    given."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", (torch.float16, torch.bfloat16), 4, dev)
+    _need(out, "out", q.dtype, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S, k, Hq, D = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != S or context_lens.shape[0] != S or D != k_cache.shape[3]:
+        raise ValueError("q/out/block_tables/context_lens shapes disagree")
+    need = decode_multi_split_workspace_size(S, k, Hq, D, max_context_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", device=dev)
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_decode_multi_split(_ptr(out), _ptr(q), _dtype_code(q.dtype), S, k, Hq, _ptr(k_cache),
+                                       _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1],
+                                       _ptr(context_lens), float(scale), float(kv_scale), int(max_context_len),
+                                       int(partition_size), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(dev))
+    _check("pa_decode_multi_split", rc)
 
 
 def set_check_mode(enable: bool) -> bool:

@@ -65,11 +65,15 @@ class OnGpu:
         wl = self.wl
         if partition_size:
             mcl = wl.max_context_len
-            need = pa.decode_split_workspace_size(wl.S, wl.Hq, wl.D, mcl, partition_size)
+            need = pa.decode_multi_split_workspace_size(wl.S, wl.qlen, wl.Hq, wl.D, mcl, partition_size)
             if self.ws is None or self.ws.numel() < need:
                 self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.q.device)
-            pa.decode_split(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale, mcl,
-                            partition_size, self.ws)
+            if wl.qlen > 1:
+                pa.decode_multi_split(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale,
+                                      mcl, partition_size, self.ws)
+            else:
+                pa.decode_split(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale, mcl,
+                                partition_size, self.ws)
         elif wl.qlen > 1:
             pa.decode_multi(self.out, self.q, self.kc, self.vc, self.bt, self.cl, wl.scale, wl.kv_scale)
         else:

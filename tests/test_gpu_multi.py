@@ -55,3 +55,29 @@ def test_single_token_through_multi_matches_decode():
     out = torch.empty_like(g.q).unsqueeze(1)
     _gpu.lib().decode_multi(out, g.q.unsqueeze(1).contiguous(), g.kc, g.vc, g.bt, g.cl, wl.scale)
     assert torch.equal(out[:, 0], base)
+
+
+@pytest.mark.parametrize("P", [64, 512])
+@pytest.mark.parametrize("case", [CASES[0], CASES[4], CASES[5], CASES[6]],
+                         ids=lambda c: "Hq%d-Hkv%d-D%d-%s-%s-k%d" % c)
+def test_multi_token_split_decode(case, P):
+    """pa_decode_multi_split: the same causal result, per partition and
+    merged by log-sum-exp; a partition wholly after a new token's position
+    (L = 65 or 513 with k > 1) contributes nothing to it."""
+    Hq, Hkv, D, qd, kd, k = case
+    wl = W.make_workload(name="t", seed=33, context_lens=LENS, Hq=Hq, Hkv=Hkv, D=D, bs=16, q_dtype=qd,
+                         kv_dtype=kd, qlen=k)
+    g = _gpu.OnGpu(wl)
+    out = g.step(partition_size=P).clone()
+    torch.cuda.synchronize()
+    kc, vc = _gpu.oracle_pool(wl)
+    want = _gpu.oracle_out(wl, kc, vc, partition_size=P)
+    assert _gpu.max_err(out, want) <= _gpu.tolerance(wl)
+    L = wl.context_lens
+    for s in range(wl.S):
+        for j in range(k):
+            if L[s] - k + j < 0:
+                assert torch.all(out[s, j] == 0)
+    assert torch.equal(g.decode(partition_size=P), out)  # deterministic
+    one_pass = g.decode().clone()
+    assert _gpu.max_err(one_pass, want) <= _gpu.tolerance(wl)
