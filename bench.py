@@ -117,6 +117,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -131,7 +132,14 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, begin: bool):
+        """Brackets the timed region: only samples that arrive inside it count."""
+        if begin:
+            self.t0 = time.perf_counter()
+        else:
+            self.t1 = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
@@ -144,7 +152,12 @@ class ClockSampler:
         self.thread.join(timeout=5)
         sm, mx, reasons, watts = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        lines = [ln for t, ln in self.lines if t0 is None or t1 is None or t0 <= t <= t1 + 0.05]
+        if not lines and self.lines:  # a region shorter than the sampling period: the nearest sample after it began
+            later = [ln for t, ln in self.lines if t0 is None or t >= t0]
+            lines = later[:1] if later else [self.lines[-1][1]]
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 8:
                 continue
@@ -318,6 +331,8 @@ def run_ours(args, wl, world, rank, local, pg):
     barrier(pg)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
+    if sampler:
+        sampler.mark(True)
     for i in range(K):
         if flush is not None:
             flush.fill_(i & 0xFF)
@@ -330,6 +345,8 @@ def run_ours(args, wl, world, rank, local, pg):
     torch.cuda.synchronize(dev)
     barrier(pg)
     wall = time.perf_counter() - t_wall
+    if sampler:
+        sampler.mark(False)
     clocks = sampler.stop() if sampler else None
     step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
     dec_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
@@ -450,6 +467,7 @@ def run_blocks(args, local):
     if sampler:
         sampler.start()
         time.sleep(0.3)
+        sampler.mark(True)
     for name, fn in (("copy_blocks", lambda: pa.copy_blocks(kc, vc, pairs)),
                      ("gather_to_host", lambda: pa.gather_blocks(host, kc, vc, ids)),
                      ("scatter_from_host", lambda: pa.scatter_blocks(kc, vc, host, ids))):
@@ -465,6 +483,8 @@ def run_blocks(args, local):
         torch.cuda.synchronize()
         us = 1e3 * e0.elapsed_time(e1) / K
         res[name] = {"us": us, "gbs": 2 * moved / (us * 1e-6) / 1e9}
+    if sampler:
+        sampler.mark(False)
     clocks = sampler.stop() if sampler else None
     # KV fragmentation of the host block manager on the gqa8b length mix:
     # unused tail slots over all slots of the blocks the sequences hold
@@ -535,12 +555,15 @@ def run_prefill(args, local):
     if sampler:
         sampler.start()
         time.sleep(0.3)
+        sampler.mark(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(K):
         run()
     e1.record()
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
     clocks = sampler.stop() if sampler else None
     us = 1e3 * e0.elapsed_time(e1) / K
     tflops = flops / (us * 1e-6) / 1e12
