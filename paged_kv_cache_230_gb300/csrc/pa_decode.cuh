@@ -351,13 +351,12 @@ __device__ __forceinline__ float warp_factor(const float* ml, int w, int g) {
   return M == -CUDART_INF_F ? 0.f : ex2(ml[(w * NG + g) * 2] - M);
 }
 
-// CTAs per SM the register budget is sized for: the widest variants (16
-// heads per MMA, or 3 heads on the shuffle path with 128 channels) hold too
-// many accumulators for three.
+// CTAs per SM the register budget is sized for: the 3-head shuffle variant
+// with 128 channels holds too many accumulators for three (the 16-column MMA
+// variant splits its columns over warp pairs instead).
 template <int D, bool USE_MMA, int NG>
 constexpr int decode_min_ctas() {
-  return ((USE_MMA && NG > 8) || (!USE_MMA && NG > 1 && D > 64)) ? (kMinCtasPerSm < 2 ? kMinCtasPerSm : 2)
-                                                                 : kMinCtasPerSm;
+  return (!USE_MMA && NG > 1 && D > 64) ? (kMinCtasPerSm < 2 ? kMinCtasPerSm : 2) : kMinCtasPerSm;
 }
 
 template <int KV, int D, bool USE_MMA, int NG>
@@ -524,12 +523,22 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     constexpr int NT = NG / 8;   // head tiles of 8
     constexpr int KS = D / 16;   // 16-wide k-steps (and 16-row output tiles)
     constexpr bool BF = (KV == kBF16);
-    uint32_t qf[KS][NT][2];
+    // 16 columns: the warps split them, warp cw taking column tile cw & 1 for
+    // the 32 tokens (cw >> 1) * 32 .. +31 of every stage, which halves its
+    // accumulators and q fragments so that three CTAs fit per SM.  8 columns:
+    // warp cw takes all of them for tokens cw * 16 .. +15.
+    constexpr bool CSPLIT = NT == 2;
+    constexpr int NTW = CSPLIT ? 1 : NT;   // column tiles per warp
+    constexpr int NSUB = CSPLIT ? 2 : 1;   // 16-token sub-tiles per warp and stage
+    static_assert(!CSPLIT || NCW % 2 == 0, "column split pairs the consumer warps");
+    const int ct = CSPLIT ? (cw & 1) : 0;  // this warp's first column tile
+    const int rowbase = CSPLIT ? (cw >> 1) * 32 : cw * 16;
+    uint32_t qf[KS][NTW][2];
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float* qg = qbuf + (nt * 8 + qr) * D;
+      for (int nt = 0; nt < NTW; ++nt) {
+        const float* qg = qbuf + ((ct + nt) * 8 + qr) * D;
         if constexpr (KV == kE4M3) {
           const int d = 16 * j + 4 * qc;  // k order of the widened FP8 fragments
           qf[j][nt][0] = pack2<false>(qg[d] * qmul, qg[d + 1] * qmul);
@@ -542,10 +551,10 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
       }
     }
     named_bar_sync(1, NCW * 32);  // qbuf is free: it becomes the epilogue area
-    float m_run[NT][2], l_run[NT][2], oacc[KS][NT][4];
+    float m_run[NTW][2], l_run[NTW][2], oacc[KS][NTW][4];
     auto reset = [&]() {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < NTW; ++nt) {
         m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
         l_run[nt][0] = l_run[nt][1] = 0.f;
 #pragma unroll
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     // (m, l) of this warp to ml[], then its rescaled output into `area` on its turn
     auto epilogue = [&](int seg, bool last) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           float l = l_run[nt][c2];
@@ -563,23 +572,31 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
           l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
           if (qr == 0) {
-            const int g = nt * 8 + 2 * qc + c2;
+            const int g = (ct + nt) * 8 + 2 * qc + c2;
             ml[(cw * NG + g) * 2] = m_run[nt][c2];
             ml[(cw * NG + g) * 2 + 1] = l;
+            if constexpr (CSPLIT) {  // the other tile's columns: nothing from this warp
+              const int go = ((ct ^ 1) + nt) * 8 + 2 * qc + c2;
+              ml[(cw * NG + go) * 2] = -CUDART_INF_F;
+              ml[(cw * NG + go) * 2 + 1] = 0.f;
+            }
           }
         }
       }
       segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, chunk},
                               vscale, [&](bool first) {
+        // with split columns, the first warp in order that owns a column
+        // (cw 0 or 1) initialises it and the other (cw 2 or 3) adds
+        const bool fst = CSPLIT ? (cw < 2) : first;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float f0 = warp_factor<NG>(ml, cw, nt * 8 + 2 * qc);
-          const float f1 = warp_factor<NG>(ml, cw, nt * 8 + 2 * qc + 1);
+        for (int nt = 0; nt < NTW; ++nt) {
+          const float f0 = warp_factor<NG>(ml, cw, (ct + nt) * 8 + 2 * qc);
+          const float f1 = warp_factor<NG>(ml, cw, (ct + nt) * 8 + 2 * qc + 1);
 #pragma unroll
           for (int mt = 0; mt < KS; ++mt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int g = nt * 8 + 2 * qc + (e & 1);
+              const int g = (ct + nt) * 8 + 2 * qc + (e & 1);
               int d;
               if constexpr (KV == kE4M3) {
                 d = 16 * mt + 4 * (qr >> 1) + (qr & 1) + (e >= 2 ? 2 : 0);
@@ -587,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
                 d = 16 * mt + qr + (e >= 2 ? 8 : 0);
               }
               const float v = oacc[mt][nt][e] * ((e & 1) ? f1 : f0);
-              area[g * D + d] = first ? v : area[g * D + d] + v;
+              area[g * D + d] = fst ? v : area[g * D + d] + v;
             }
           }
         }
@@ -595,12 +612,12 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     };
     // token limit of each of this lane's query columns: new token j of qlen
     // sits at position L - qlen + j and attends to positions up to itself
-    int lim[NT][2];
+    int lim[NTW][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        const int n = nt * 8 + 2 * qc + c2;
+        const int n = (ct + nt) * 8 + 2 * qc + c2;
         lim[nt][c2] = n < ncol ? min(tok_end, L - p.qlen + n / p.G + 1) : tok_end;
       }
     reset();
@@ -611,67 +628,86 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
-      const int slice0 = tok_begin + t * TILE + row0;  // first token of this warp's 16
-      const int n_valid = min(16, tok_end - slice0);
-      if (n_valid > 0) {
+      const int slice0 = tok_begin + t * TILE + rowbase;  // first token of this warp's rows
+      int n_valid[NSUB];
+#pragma unroll
+      for (int u = 0; u < NSUB; ++u) n_valid[u] = min(16, tok_end - (slice0 + 16 * u));
+      if (n_valid[0] > 0) {
         const uint32_t kst = ring_u32 + stage * Gm::STAGE_BYTES;
         const uint32_t vst = kst + Gm::HALF_BYTES;
-        float sacc[NT][4];
+        float sacc[NSUB][NTW][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-        // ---- S^T = K Q^T ----
-        if constexpr (KV != kE4M3) {
-          const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        for (int u = 0; u < NSUB; ++u)
 #pragma unroll
-          for (int j = 0; j < KS; ++j) {
-            const int cb = 32 * j;
-            const int sg = cb / Gm::BOXB, c = (cb % Gm::BOXB) / 16 + (lane >> 4);
-            uint32_t a[4];
-            ldsm_x4(kst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + c * 16), a[0], a[1], a[2], a[3]);
+          for (int nt = 0; nt < NTW; ++nt) sacc[u][nt][0] = sacc[u][nt][1] = sacc[u][nt][2] = sacc[u][nt][3] = 0.f;
+        // ---- S^T = K Q^T, per 16-token sub-tile ----
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816<BF>(sacc[nt], a, qf[j][nt][0], qf[j][nt][1]);
-          }
-        } else {
-          const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        for (int u = 0; u < NSUB; ++u) {
+          if (u > 0 && n_valid[u] <= 0) continue;
+          const int row0 = rowbase + 16 * u;
+          if constexpr (KV != kE4M3) {
+            const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-          for (int j = 0; j < KS; j += 2) {
-            const int c = j + (lane >> 4);
-            uint32_t R[4];
-            ldsm_x4(kst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int j = 0; j < KS; ++j) {
+              const int cb = 32 * j;
+              const int sg = cb / Gm::BOXB, c = (cb % Gm::BOXB) / 16 + (lane >> 4);
               uint32_t a[4];
-              a[0] = e4m3x2_to_f16x2(R[2 * kk]);
-              a[2] = e4m3x2_to_f16x2(R[2 * kk] >> 16);
-              a[1] = e4m3x2_to_f16x2(R[2 * kk + 1]);
-              a[3] = e4m3x2_to_f16x2(R[2 * kk + 1] >> 16);
+              ldsm_x4(kst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + c * 16), a[0], a[1], a[2], a[3]);
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma16816<false>(sacc[nt], a, qf[j + kk][nt][0], qf[j + kk][nt][1]);
+              for (int nt = 0; nt < NTW; ++nt) mma16816<BF>(sacc[u][nt], a, qf[j][nt][0], qf[j][nt][1]);
+            }
+          } else {
+            const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int j = 0; j < KS; j += 2) {
+              const int c = j + (lane >> 4);
+              uint32_t R[4];
+              ldsm_x4(kst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(R[2 * kk]);
+                a[2] = e4m3x2_to_f16x2(R[2 * kk] >> 16);
+                a[1] = e4m3x2_to_f16x2(R[2 * kk + 1]);
+                a[3] = e4m3x2_to_f16x2(R[2 * kk + 1] >> 16);
+#pragma unroll
+                for (int nt = 0; nt < NTW; ++nt)
+                  mma16816<false>(sacc[u][nt], a, qf[j + kk][nt][0], qf[j + kk][nt][1]);
+              }
             }
           }
         }
-        // ---- online softmax over this warp's 16 tokens ----
-        uint32_t pb[NT][2];
+        // ---- online softmax over this warp's NSUB x 16 tokens ----
+        uint32_t pb[NSUB][NTW][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float sv[4], alpha[2];
+        for (int nt = 0; nt < NTW; ++nt) {
+          float sv[NSUB][4], alpha[2];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = qr + (e >= 2 ? 8 : 0);
-            sv[e] = slice0 + row < lim[nt][e & 1] ? sacc[nt][e] * qk_mult : -CUDART_INF_F;
-          }
+          for (int u = 0; u < NSUB; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int row = 16 * u + qr + (e >= 2 ? 8 : 0);
+              sv[u][e] = slice0 + row < lim[nt][e & 1] ? sacc[u][nt][e] * qk_mult : -CUDART_INF_F;
+            }
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
-            float mx = fmaxf(sv[c2], sv[c2 + 2]);
+            float mx = fmaxf(sv[0][c2], sv[0][c2 + 2]);
+#pragma unroll
+            for (int u = 1; u < NSUB; ++u) mx = fmaxf(mx, fmaxf(sv[u][c2], sv[u][c2 + 2]));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
             const float m_new = fmaxf(m_run[nt][c2], mx);
             const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
             alpha[c2] = ex2(m_run[nt][c2] - m_use);
-            sv[c2] = ex2(sv[c2] - m_use);
-            sv[c2 + 2] = ex2(sv[c2 + 2] - m_use);
-            l_run[nt][c2] = l_run[nt][c2] * alpha[c2] + (sv[c2] + sv[c2 + 2]);
+            float add = 0.f;
+#pragma unroll
+            for (int u = 0; u < NSUB; ++u) {
+              sv[u][c2] = ex2(sv[u][c2] - m_use);
+              sv[u][c2 + 2] = ex2(sv[u][c2 + 2] - m_use);
+              add += sv[u][c2] + sv[u][c2 + 2];
+            }
+            l_run[nt][c2] = l_run[nt][c2] * alpha[c2] + add;
             m_run[nt][c2] = m_new;
           }
 #pragma unroll
@@ -682,42 +718,50 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
             oacc[mt][nt][3] *= alpha[1];
           }
           // P^T fragment (rows = tokens) -> transposed into the B operand of the PV product
-          pb[nt][0] = movm_t(pack2<BF>(sv[0], sv[1]));
-          pb[nt][1] = movm_t(pack2<BF>(sv[2], sv[3]));
-        }
-        // ---- O^T += V^T P^T ----
-        if constexpr (KV != kE4M3) {
-          const int r = row0 + (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            const int cb = 32 * mt;
-            const int sg = cb / Gm::BOXB, c = (cb % Gm::BOXB) / 16 + ((lane >> 3) & 1);
-            uint32_t a[4];
-            ldsm_x4_t(vst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + c * 16), a[0], a[1], a[2], a[3]);
-            if (n_valid < 16) mask_tokens(a, lane, n_valid);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816<BF>(oacc[mt][nt], a, pb[nt][0], pb[nt][1]);
+          for (int u = 0; u < NSUB; ++u) {
+            pb[u][nt][0] = movm_t(pack2<BF>(sv[u][0], sv[u][1]));
+            pb[u][nt][1] = movm_t(pack2<BF>(sv[u][2], sv[u][3]));
           }
-        } else {
-          const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        }
+        // ---- O^T += V^T P^T, per 16-token sub-tile ----
 #pragma unroll
-          for (int j = 0; j < KS; j += 2) {
-            const int c = j + (lane >> 4);
-            uint32_t R[4];
-            ldsm_x4(vst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
+        for (int u = 0; u < NSUB; ++u) {
+          if (u > 0 && n_valid[u] <= 0) continue;
+          const int row0 = rowbase + 16 * u;
+          if constexpr (KV != kE4M3) {
+            const int r = row0 + (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              // rows = tokens, columns = channels; transposing the widened 8x8
-              // pieces yields V^T fragments whose 16 rows are the channels
-              // 16j' + {0,1,4,5,8,9,12,13} (low) and {2,3,6,7,10,11,14,15} (high)
+            for (int mt = 0; mt < KS; ++mt) {
+              const int cb = 32 * mt;
+              const int sg = cb / Gm::BOXB, c = (cb % Gm::BOXB) / 16 + ((lane >> 3) & 1);
               uint32_t a[4];
-              a[0] = movm_t(e4m3x2_to_f16x2(R[2 * kk]));
-              a[1] = movm_t(e4m3x2_to_f16x2(R[2 * kk] >> 16));
-              a[2] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1]));
-              a[3] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1] >> 16));
-              if (n_valid < 16) mask_tokens(a, lane, n_valid);
+              ldsm_x4_t(vst + sg * Gm::SEG_BYTES + swz<Gm>(r * Gm::BOXB + c * 16), a[0], a[1], a[2], a[3]);
+              if (n_valid[u] < 16) mask_tokens(a, lane, n_valid[u]);
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma16816<false>(oacc[j + kk][nt], a, pb[nt][0], pb[nt][1]);
+              for (int nt = 0; nt < NTW; ++nt) mma16816<BF>(oacc[mt][nt], a, pb[u][nt][0], pb[u][nt][1]);
+            }
+          } else {
+            const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int j = 0; j < KS; j += 2) {
+              const int c = j + (lane >> 4);
+              uint32_t R[4];
+              ldsm_x4(vst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                // rows = tokens, columns = channels; transposing the widened 8x8
+                // pieces yields V^T fragments whose 16 rows are the channels
+                // 16j' + {0,1,4,5,8,9,12,13} (low) and {2,3,6,7,10,11,14,15} (high)
+                uint32_t a[4];
+                a[0] = movm_t(e4m3x2_to_f16x2(R[2 * kk]));
+                a[1] = movm_t(e4m3x2_to_f16x2(R[2 * kk] >> 16));
+                a[2] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1]));
+                a[3] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1] >> 16));
+                if (n_valid[u] < 16) mask_tokens(a, lane, n_valid[u]);
+#pragma unroll
+                for (int nt = 0; nt < NTW; ++nt) mma16816<false>(oacc[j + kk][nt], a, pb[u][nt][0], pb[u][nt][1]);
+              }
             }
           }
         }
