@@ -504,12 +504,17 @@ def run_blocks(args, local):
     print(json.dumps(line), flush=True)
 
 
-def measured_tensor_peak():
+def measured_tensor_peak(sustained: bool = False):
+    """bf16 tensor peak: the burst figure, or the sustained one (a seconds-long
+    loop under the power cap) for kernels timed inside a long loop."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured"
+            d = json.load(f)
+        if sustained and "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+        return float(d["bf16_tflops"]), "measured"
     except (OSError, KeyError, ValueError):
-        return 1900.0, "fallback"
+        return (1700.0, "fallback (sustained)") if sustained else (1900.0, "fallback")
 
 
 def run_prefill(args, local):
@@ -567,14 +572,19 @@ def run_prefill(args, local):
     clocks = sampler.stop() if sampler else None
     us = 1e3 * e0.elapsed_time(e1) / K
     tflops = flops / (us * 1e-6) / 1e12
-    peak, kind = measured_tensor_peak()
+    # the timed region is about two seconds of back-to-back launches under
+    # the power cap, so the sustained peak is the denominator; the burst
+    # fraction is reported beside it
+    peak, kind = measured_tensor_peak(sustained=True)
+    burst, _ = measured_tensor_peak()
     line = {"metric": "paged prefill attention TFLOP/s (causal FLOPs)", "value": tflops, "unit": "TFLOP/s",
             "n_gpus": 1, "steps": K, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": wl.name, "num_seqs": S, "chunk": C, "context": L,
                                             "q_heads": 32, "kv_heads": 8, "head_dim": 128, "block_size": bs},
             "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6), "clocks": clocks,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "peak_source": kind, "kernel": "pa_prefill"}}
+                         "frac": tflops / peak, "peak_source": kind, "frac_of_burst_peak": tflops / burst,
+                         "kernel": "pa_prefill"}}
     print(json.dumps(line), flush=True)
 
 
