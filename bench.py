@@ -534,8 +534,7 @@ def run_prefill(args, local):
     C = args.qlen if args.qlen > 1 else 2048
     L = 2 * C
     bs = getattr(args, "block_size", 16)
-    wl = W.make_workload(name="prefill_gqa8b", seed=7, context_lens=[L] * S, Hq=32, Hkv=8, D=128, bs=bs,
-                         q_dtype="bf16", kv_dtype="bf16", qlen=C)
+    wl = W.make_prefill_workload(S=S, C=C, bs=bs)
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
     flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())

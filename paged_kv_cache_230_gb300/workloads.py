@@ -392,6 +392,16 @@ def make_config(idx: int, seed: Optional[int] = None, fill_unused: str = "normal
     raise ValueError(idx)
 
 
+def make_prefill_workload(S: int = 16, C: int = 2048, bs: int = 16, seed: int = 7,
+                          fill_unused: str = "normal") -> Workload:
+    """The chunked-prefill batch: S sequences, each with a chunk of C new
+    tokens at the end of a context of 2C (so every query attends to between
+    C + 1 and 2C tokens), GQA-8B heads (32 query / 8 kv heads), head_dim 128,
+    bf16, block size bs."""
+    return make_workload(name="prefill_gqa8b", seed=seed, context_lens=[2 * C] * S, Hq=32, Hkv=8, D=128, bs=bs,
+                         q_dtype=BF16, kv_dtype=BF16, qlen=C, fill_unused=fill_unused)
+
+
 def subset(wl: Workload, seqs) -> Workload:
     """The same pool with only the chosen sequences (for sampled oracle checks)."""
     seqs = np.asarray(seqs, dtype=np.int64)

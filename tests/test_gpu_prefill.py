@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_230_gb300 import workloads as W
 from tests import _gpu
 
@@ -38,3 +39,118 @@ def test_prefill_matches_oracle(case):
     for s, L in enumerate(lens):
         for j in range(max(0, C - L)):
             assert torch.all(out[s, j] == 0)
+
+
+def _prefill(g, wl, bt=None, kc=None, vc=None, cl=None):
+    out = torch.full_like(g.q, float("nan"))
+    _gpu.lib().prefill(out, g.q, g.kc if kc is None else kc, g.vc if vc is None else vc,
+                       g.bt if bt is None else bt, g.cl if cl is None else cl, wl.scale)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_full_size_bench_batch_on_sampled_rows():
+    """The batch bench.py times (16 x 2048 new tokens at context 4096, 32/8
+    heads, bf16, block size 16), in the same launch, checked on sampled query
+    rows that the oracle evaluates one by one; every output is finite."""
+    wl = W.make_prefill_workload()
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    out = _prefill(g, wl)
+    assert _gpu.lib().get_device_error() == 0
+    assert torch.isfinite(out.float()).all()
+    S, C = wl.S, wl.qlen
+    rng = np.random.default_rng(11)
+    s_idx = np.concatenate([rng.integers(0, S, 60), [0, S - 1, 5, 5, 9]])
+    j_idx = np.concatenate([rng.integers(0, C, 60), [0, C - 1, 127, 128, 1919]])
+    kc, vc = _gpu.oracle_pool(wl)
+    q_sub = np.ascontiguousarray(wl.q[s_idx, j_idx])  # [n, Hq, D]
+    L_sub = (wl.context_lens[s_idx] - C + 1 + j_idx).astype(np.int32)
+    want = oracle.decode(q_sub, wl.q_dtype, kc, vc, wl.kv_dtype, np.ascontiguousarray(wl.block_tables[s_idx]),
+                         L_sub, wl.scale, wl.kv_scale)
+    got = out[torch.from_numpy(s_idx).cuda(), torch.from_numpy(j_idx).cuda()]
+    assert _gpu.max_err(got, want) <= _gpu.tolerance(wl)
+
+
+def test_unused_slots_holding_nan_are_never_read():
+    """Pool slots past every context hold NaN: the last K/V tile reaches into
+    them, and neither scores nor P.V may pick them up."""
+    wl = W.make_workload(name="t", seed=43, context_lens=[130, 300, 17, 1000], Hq=8, Hkv=2, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=130, fill_unused="nan")
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    out = _prefill(g, wl)
+    kc, vc = _gpu.oracle_pool(wl)
+    assert _gpu.max_err(out, _gpu.oracle_out(wl, kc, vc)) <= _gpu.tolerance(wl)
+
+
+def test_block_placement_is_bit_invariant():
+    """Moving every block to another physical id changes no output bit, and
+    the result is the same from run to run."""
+    wl = W.make_workload(name="t", seed=44, context_lens=[256, 700, 129], Hq=8, Hkv=2, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=256)
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    base = _prefill(g, wl)
+    assert torch.equal(_prefill(g, wl), base)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(wl.NB)).cuda()
+    kc2 = torch.empty_like(g.kc)
+    vc2 = torch.empty_like(g.vc)
+    kc2[perm] = g.kc
+    vc2[perm] = g.vc
+    bt2 = torch.where(g.bt >= 0, perm[g.bt.clamp(min=0).long()].int(), g.bt)
+    assert torch.equal(_prefill(g, wl, bt=bt2, kc=kc2, vc=vc2), base)
+
+
+def test_single_new_token_and_empty_batch():
+    wl = W.make_workload(name="t", seed=45, context_lens=[1, 64, 129], Hq=4, Hkv=2, D=128, bs=16,
+                         q_dtype="f16", kv_dtype="f16", qlen=1)
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    q = g.q.unsqueeze(1).contiguous()  # one new token: [S, 1, Hq, D]
+    out = torch.full_like(q, float("nan"))
+    _gpu.lib().prefill(out, q, g.kc, g.vc, g.bt, g.cl, wl.scale)
+    torch.cuda.synchronize()
+    kc, vc = _gpu.oracle_pool(wl)
+    assert _gpu.max_err(out[:, 0], _gpu.oracle_out(wl, kc, vc)) <= _gpu.tolerance(wl)
+    empty = torch.empty((0, 4, 4, 128), dtype=torch.float16, device="cuda")
+    _gpu.lib().prefill(empty, empty, g.kc, g.vc, g.bt[:0], g.cl[:0], wl.scale)
+
+
+def test_unsupported_and_invalid_arguments_launch_nothing():
+    pa = _gpu.lib()
+    q = torch.zeros((1, 4, 2, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    cl = torch.full((1,), 4, dtype=torch.int32, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:  # head_dim 64: the prefill kernel is built for 128
+        pa.prefill(q.clone(), q, kc, kc, bt, cl, 0.1)
+    assert e.value.status == -2
+    q = torch.zeros((1, 4, 2, 128), dtype=torch.bfloat16, device="cuda")
+    k8 = torch.zeros((4, 2, 16, 128), dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:  # FP8 caches: decode only
+        pa.prefill(q.clone(), q, k8, k8, bt, cl, 0.1)
+    assert e.value.status == -2
+    kc = torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    for bad in (0.0, -1.0, float("nan")):
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.prefill(q.clone(), q, kc, kc, bt, cl, bad)
+        assert e.value.status == -1
+
+
+def test_out_of_range_block_ids_are_contained_and_reported():
+    pa = _gpu.lib()
+    wl = W.make_workload(name="t", seed=46, context_lens=[200, 300], Hq=4, Hkv=2, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=128)
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    assert pa.get_device_error() == 0
+    bad = g.bt.clone()
+    bad[1, 3] = wl.NB + 5
+    out = _prefill(g, wl, bt=bad)
+    assert pa.get_device_error() & pa.DEVERR_BLOCK_ID
+    assert pa.get_device_error() == 0  # reading clears it
+    assert torch.isfinite(out.float()).all()
+    # the sequence that never touches the bad entry is unaffected
+    base = _prefill(g, wl)
+    assert torch.equal(out[0], base[0])
