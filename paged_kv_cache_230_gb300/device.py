@@ -55,6 +55,22 @@ class DeviceBatch:
                                                         self.partition_size)
             self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=d)
 
+    INPUTS = ("q", "key", "value", "block_tables", "context_lens", "slot_mapping", "out")
+
+    def io_set(self) -> dict:
+        """The per-step input and output tensors the batch is bound to."""
+        return {name: getattr(self, name) for name in self.INPUTS}
+
+    def spare_io_set(self) -> dict:
+        """A second set of per-step input and output tensors of the same shapes
+        (the KV pool and workspace stay shared), for overlapping one step's
+        copies with another step's kernels."""
+        return {name: torch.empty_like(t) for name, t in self.io_set().items()}
+
+    def bind(self, io: dict) -> None:
+        for name in self.INPUTS:
+            setattr(self, name, io[name])
+
     def scatter(self) -> None:
         pa.reshape_and_cache(self.key, self.value, self.k_cache, self.v_cache, self.slot_mapping,
                              self.wl.kv_scale)
