@@ -101,10 +101,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Two E4M3 codes (low byte = first element) -> f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return uint32_t(r.x) | (uint32_t(r.y) << 16);
+// Four E4M3 codes (low byte = first element) widened exactly to two f16x2
+// words: codes 0, 1 to `lo`, codes 2, 3 to `hi`.  The conversion instruction
+// reads each 16-bit half directly; masking and shifting the word for a
+// conversion helper cost as much as the conversions.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 c0, c1;\n\t"
+      "mov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(four));
 }
 
 // Zero the halves of an A fragment whose token index (k) is >= n_valid.
@@ -142,10 +148,11 @@ __device__ __forceinline__ void load_piece(const uint8_t* src, float* f) {
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
+        uint32_t h2[2];
+        e4m3x4_to_f16x2x2(w[i], h2[0], h2[1]);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const uint32_t h2 = e4m3x2_to_f16x2(w[i] >> (16 * j));
-          const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2[j]));
           f[4 * i + 2 * j] = v.x;
           f[4 * i + 2 * j + 1] = v.y;
         }
@@ -157,10 +164,11 @@ __device__ __forceinline__ void load_piece(const uint8_t* src, float* f) {
     const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
+      uint32_t h2[2];
+      e4m3x4_to_f16x2x2(w[i], h2[0], h2[1]);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const uint32_t h2 = e4m3x2_to_f16x2(w[i] >> (16 * j));
-        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2[j]));
         f[4 * i + 2 * j] = v.x;
         f[4 * i + 2 * j + 1] = v.y;
       }
@@ -666,10 +674,8 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
 #pragma unroll
               for (int kk = 0; kk < 2; ++kk) {
                 uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(R[2 * kk]);
-                a[2] = e4m3x2_to_f16x2(R[2 * kk] >> 16);
-                a[1] = e4m3x2_to_f16x2(R[2 * kk + 1]);
-                a[3] = e4m3x2_to_f16x2(R[2 * kk + 1] >> 16);
+                e4m3x4_to_f16x2x2(R[2 * kk], a[0], a[2]);
+                e4m3x4_to_f16x2x2(R[2 * kk + 1], a[1], a[3]);
 #pragma unroll
                 for (int nt = 0; nt < NTW; ++nt)
                   mma16816<false>(sacc[u][nt], a, qf[j + kk][nt][0], qf[j + kk][nt][1]);
@@ -753,11 +759,13 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
                 // rows = tokens, columns = channels; transposing the widened 8x8
                 // pieces yields V^T fragments whose 16 rows are the channels
                 // 16j' + {0,1,4,5,8,9,12,13} (low) and {2,3,6,7,10,11,14,15} (high)
-                uint32_t a[4];
-                a[0] = movm_t(e4m3x2_to_f16x2(R[2 * kk]));
-                a[1] = movm_t(e4m3x2_to_f16x2(R[2 * kk] >> 16));
-                a[2] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1]));
-                a[3] = movm_t(e4m3x2_to_f16x2(R[2 * kk + 1] >> 16));
+                uint32_t a[4], w0, w1, w2, w3;
+                e4m3x4_to_f16x2x2(R[2 * kk], w0, w1);
+                e4m3x4_to_f16x2x2(R[2 * kk + 1], w2, w3);
+                a[0] = movm_t(w0);
+                a[1] = movm_t(w1);
+                a[2] = movm_t(w2);
+                a[3] = movm_t(w3);
                 if (n_valid[u] < 16) mask_tokens(a, lane, n_valid[u]);
 #pragma unroll
                 for (int nt = 0; nt < NTW; ++nt) mma16816<false>(oacc[j + kk][nt], a, pb[u][nt][0], pb[u][nt][1]);
