@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="time the scatter and the decode as two launches instead of pa_cache_and_decode")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
     ap.add_argument("--qlen", type=int, default=1, help="new query tokens per sequence (multi-token decode)")
@@ -308,10 +310,12 @@ def run_ours(args, wl, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     P = wl.partition_size if args.split < 0 else args.split
-    b = DeviceBatch(wl, dev, partition_size=P)
+    fused = not args.separate
+    b = DeviceBatch(wl, dev, partition_size=P, fused=fused)
     stream = torch.cuda.current_stream(dev)
     kv_bytes = wl.kv_bytes()
-    alg_bytes = wl.algorithmic_bytes()
+    # the fused kernel also reads the new rows and writes them into the pool
+    alg_bytes = wl.algorithmic_bytes() + (wl.scatter_bytes() if fused else 0)
     flush = None
     unique_bytes = int(wl.notes.get("unique_blocks", 0)) * wl.Hkv * wl.bs * wl.D * 2 * W.ELEM_BYTES[wl.kv_dtype]
     if unique_bytes < 4 * L2_BYTES:
@@ -338,9 +342,13 @@ def run_ours(args, wl, world, rank, local, pg):
             flush.fill_(i & 0xFF)
         e0, e1, e2 = ev[i]
         e0.record(stream)
-        b.scatter()
-        e1.record(stream)
-        b.decode()
+        if fused:  # one launch: e1 marks the (empty) scatter slot
+            e1.record(stream)
+            b.step()
+        else:
+            b.scatter()
+            e1.record(stream)
+            b.decode()
         e2.record(stream)
     torch.cuda.synchronize(dev)
     barrier(pg)
@@ -361,6 +369,8 @@ def run_ours(args, wl, world, rank, local, pg):
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
     kernel_name = ("decode_multi_split" if P else "decode_multi") if wl.qlen > 1 else ("decode_split" if P else "decode")
+    if fused:
+        kernel_name = "cache_and_" + kernel_name
     traffic = recorded_traffic(wl.name, kernel_name)
 
     e2e = None
@@ -386,7 +396,9 @@ def run_ours(args, wl, world, rank, local, pg):
                        "context_tokens": int(wl.context_lens.sum()), "max_context": wl.max_context_len,
                        "kv_bytes_per_step": kv_bytes, "partition_size": P,
                        "l2": "inputs larger than L2" if flush is None else "256 MiB L2 flush between steps",
-                       "parallelism": "replicas" if world > 1 else "single"},
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "step": ("pa_cache_and_decode: scatter fused into the decode launch" if fused
+                                else "pa_reshape_and_cache, then the decode call")},
             "decode_tokens_per_s": seqs / (ms_per_step * 1e-3),
             "pct_of_hbm_peak": 100.0 * value / peak,
             "decode_kernel_us": 1e3 * dec_avg,

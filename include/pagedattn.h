@@ -213,6 +213,33 @@ PA_API int pa_decode_multi_split(void *out, const void *q, int32_t q_dtype, int3
                                  void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_cache_and_decode: pa_reshape_and_cache of this step's new rows followed
+ * by pa_decode_multi (partition_size 0) or pa_decode_multi_split
+ * (partition_size > 0), in one launch: the CTA that attends over a new
+ * token's position writes that token's K and V rows for its kv head into
+ * the pool before it loads any tile, so the step needs no separate scatter
+ * kernel.  The result and the pool bytes are the same as the two calls'.
+ *   key, value    [num_seqs * num_q_tokens, num_kv_heads, head_dim] of q_dtype,
+ *                 16-byte aligned; row s * num_q_tokens + j is new token j of
+ *                 sequence s (position context_lens[s] - num_q_tokens + j)
+ *   slot_mapping  int64 [num_seqs * num_q_tokens]: the slot of that row (as
+ *                 pa_reshape_and_cache); negative = skip.  It must be the
+ *                 position's slot in the sequence's own block table (a block
+ *                 private to the sequence, as copy-on-write makes it); a slot
+ *                 outside the pool is skipped, and either case sets
+ *                 PA_DEVERR_SLOT.
+ * Other arguments as pa_decode_multi / pa_decode_multi_split (workspace and
+ * max_context_len are read only when partition_size > 0).
+ */
+PA_API int pa_cache_and_decode(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+                               int32_t num_q_heads, const void *key, const void *value,
+                               const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                               const pa_cache_desc *cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *context_lens, float scale, float kv_scale, int32_t max_context_len,
+                               int32_t partition_size, void *workspace, size_t workspace_bytes,
+                               pa_stream_t stream);
+
+/*
  * pa_decode_split_noalloc: pa_decode_split without a workspace argument, for
  * callers that cannot allocate device memory when they call (for example a
  * serving process whose KV-cache pool already holds nearly all of HBM, or a

@@ -369,10 +369,28 @@ size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
 
 namespace {
 
+// The new rows a fused call writes into the pool (pa_cache_and_decode).
+struct CacheWrite {
+  const void* key;
+  const void* value;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+};
+
+void set_cache_write(pa::DecodeParams& p, const CacheWrite* w) {
+  if (!w) return;
+  p.new_key = w->key;
+  p.new_value = w->value;
+  p.slot_mapping = w->slot_mapping;
+  p.k_cache = w->k_cache;
+  p.v_cache = w->v_cache;
+}
+
 // Split decode of one or several new tokens per sequence: the partition
 // kernel, then the log-sum-exp merge of the runs, on one stream.
 int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition_size, void* workspace,
-                      size_t workspace_bytes, pa_stream_t stream) {
+                      size_t workspace_bytes, pa_stream_t stream, const CacheWrite* write = nullptr) {
   int rc = check_decode(a);
   if (rc) return rc;
   if (partition_size <= 0 || partition_size % pa::kTileTokens || max_context_len < 0) return PA_ERR_INVALID_ARG;
@@ -390,6 +408,7 @@ int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t part
   if ((rc = make_cache_tensor_map(&tk, a.k_cache, cache)) || (rc = make_cache_tensor_map(&tv, a.v_cache, cache)))
     return rc;
   pa::DecodeParams p = make_params(a, err);
+  set_cache_write(p, write);
   p.partition_size = partition_size;
   p.Pmax = static_cast<int>(np);
   p.parts_per_cta = parts_per_cta(a.num_seqs, cache->num_kv_heads, p.Pmax);
@@ -414,6 +433,35 @@ int pa_decode_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
   const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, 1, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
   return decode_split_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream);
+}
+
+int pa_cache_and_decode(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
+                        int32_t num_q_heads, const void* key, const void* value, const int64_t* slot_mapping,
+                        void* k_cache, void* v_cache, const pa_cache_desc* cache, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, float kv_scale,
+                        int32_t max_context_len, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                        pa_stream_t stream) {
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, kv_scale};
+  int rc = check_decode(a);
+  if (rc) return rc;
+  if (partition_size < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value)) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_seqs) * num_q_tokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+  const CacheWrite w{key, value, slot_mapping, k_cache, v_cache};
+  if (partition_size > 0)
+    return decode_split_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream, &w);
+  if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
+    return rc;
+  pa::DecodeParams p = make_params(a, err);
+  set_cache_write(p, &w);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st), st);
 }
 
 int pa_decode_multi_split(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,

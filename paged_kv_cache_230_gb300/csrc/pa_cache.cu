@@ -6,10 +6,7 @@
 // (token, kv head, K-or-V) row, so a warp covers whole rows with coalesced
 // loads and 16-byte (16-bit cache) or 8-byte (FP8 cache) stores.  Every slot
 // is bounds-checked: a slot outside the pool is skipped and recorded.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-
+#include "pa_cache_row.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -17,11 +14,6 @@ namespace pa {
 namespace {
 
 constexpr int kErrSlot = 0x4;
-
-__device__ __forceinline__ float widen16(uint32_t bits, int dtype) {
-  return dtype == kF16 ? __half2float(__ushort_as_half(static_cast<uint16_t>(bits)))
-                       : __uint_as_float(bits << 16);
-}
 
 template <bool TO_FP8>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParams p) {
@@ -47,31 +39,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParam
   const int64_t dst = ((blk * p.Hkv + h) * p.bs + off) * p.D + chunk * 8;
   const uint16_t* in = static_cast<const uint16_t*>(which ? p.value : p.key);
   const uint4 u = *reinterpret_cast<const uint4*>(in + src);
-
-  if constexpr (!TO_FP8) {
-    uint16_t* cache = static_cast<uint16_t*>(which ? p.v_cache : p.k_cache);
-    *reinterpret_cast<uint4*>(cache + dst) = u;
-  } else {
-    uint8_t* cache = static_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    uint32_t packed[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint32_t src2 = w[2 * i + j];
-        // float32 widening is exact; the division is IEEE round-to-nearest
-        const float lo = __fdiv_rn(widen16(src2 & 0xFFFFu, p.in_dtype), p.kv_scale);
-        const float hi = __fdiv_rn(widen16(src2 >> 16, p.in_dtype), p.kv_scale);
-        const __nv_fp8x2_storage_t two =
-            __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-        word |= static_cast<uint32_t>(two) << (16 * j);
-      }
-      packed[i] = word;
-    }
-    *reinterpret_cast<uint2*>(cache + dst) = make_uint2(packed[0], packed[1]);
-  }
+  store_row_piece<TO_FP8>(u, which ? p.v_cache : p.k_cache, dst, p.in_dtype, p.kv_scale);
 }
 
 }  // namespace

@@ -38,6 +38,7 @@
 #include <cuda_fp8.h>
 #include <math_constants.h>
 
+#include "pa_cache_row.cuh"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -447,6 +448,36 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
     int base = blk_begin;
     int cur = (base + lane < blk_end) ? __ldg(bt_row + base + lane) : -1;
     int nxt = (base + 32 + lane < blk_end) ? __ldg(bt_row + base + 32 + lane) : -1;
+    if (p.new_key != nullptr) {
+      // fused cache write: this CTA's own new rows (position L - qlen + j of
+      // sequence s, kv head h, inside its token range) go to their slots
+      // before any tile load reads the pool.  A slot that is not that
+      // position's slot in the sequence's own table is written as given and
+      // flagged (the tile loads would not see it).
+      constexpr int kPieces = D / 8;  // 16-byte pieces of a 16-bit row
+      for (int i = lane; i < p.qlen * 2 * kPieces; i += 32) {
+        const int piece = i % kPieces, which = (i / kPieces) & 1, j = i / (2 * kPieces);
+        const int pos = L - p.qlen + j;
+        if (pos < tok_begin || pos >= tok_end) continue;  // before the context, or another run's part
+        const int64_t tok = static_cast<int64_t>(s) * p.qlen + j;
+        const int64_t slot = p.slot_mapping[tok];
+        if (slot < 0) continue;  // padding token
+        const bool first = piece == 0 && which == 0;
+        if (slot >= p.num_blocks * bs) {
+          if (first) atomicOr(p.err, kErrSlot);
+          continue;
+        }
+        if (first && slot != static_cast<int64_t>(__ldg(bt_row + pos / bs)) * bs + pos % bs) atomicOr(p.err, kErrSlot);
+        const int64_t blk = slot / bs, off = slot % bs;
+        const uint16_t* in = static_cast<const uint16_t*>(which ? p.new_value : p.new_key);
+        const uint4 u = *reinterpret_cast<const uint4*>(in + (tok * p.Hkv + h) * D + piece * 8);
+        store_row_piece<KV == kE4M3>(u, which ? p.v_cache : p.k_cache, ((blk * p.Hkv + h) * bs + off) * D + piece * 8,
+                                     p.q_dtype, p.kv_scale);
+      }
+      // the plain stores are visible to the tile loads (async proxy) issued next
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    }
     int t = 0;
     bool ok = true;
     for (; t < ntiles; ++t) {

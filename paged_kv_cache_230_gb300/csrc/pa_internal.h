@@ -41,6 +41,12 @@ struct DecodeParams {
   int nst;                    // ring stages (set by the launcher)
   float scale_log2;           // scale * log2(e)
   float kv_scale;             // FP8 dequantisation scale (1 for 16-bit caches)
+  // fused cache write (pa_cache_and_decode); new_key == nullptr: none
+  const void* new_key;        // [S * qlen, Hkv, D] of q_dtype
+  const void* new_value;
+  const int64_t* slot_mapping;  // [S * qlen]
+  void* k_cache;              // the pool, written through plain stores
+  void* v_cache;
 };
 
 // Launches the decode (or split-partition) kernel for one cache dtype.

@@ -26,8 +26,9 @@ def from_device16(t: torch.Tensor) -> np.ndarray:
 
 
 class DeviceBatch:
-    def __init__(self, wl: Workload, device="cuda", partition_size: Optional[int] = None):
+    def __init__(self, wl: Workload, device="cuda", partition_size: Optional[int] = None, fused: bool = True):
         self.wl = wl
+        self.fused = fused  # step() = one pa_cache_and_decode launch instead of scatter + decode
         self.device = torch.device(device)
         self.partition_size = wl.partition_size if partition_size is None else partition_size
         d = self.device
@@ -93,8 +94,16 @@ class DeviceBatch:
         return self.out
 
     def step(self) -> torch.Tensor:
-        self.scatter()
-        return self.decode()
+        if not self.fused:
+            self.scatter()
+            return self.decode()
+        wl = self.wl
+        pa.cache_and_decode(self.out, self.q, self.key, self.value, self.slot_mapping, self.k_cache, self.v_cache,
+                            self.block_tables, self.context_lens, wl.scale, wl.kv_scale, wl.max_context_len,
+                            self.partition_size, self.workspace)
+        return self.out
 
     def launches_per_step(self) -> int:
+        if self.fused:
+            return 2 if self.partition_size else 1
         return 3 if self.partition_size else 2

@@ -31,7 +31,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: 
           -7: "not enough free blocks", -8: "unknown or duplicate sequence id"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill", "pa_decode_split_workspace_size",
-           "pa_decode_split", "pa_decode_multi_split_workspace_size", "pa_decode_multi_split",
+           "pa_decode_split", "pa_decode_multi_split_workspace_size", "pa_decode_multi_split", "pa_cache_and_decode",
            "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
            "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_num_free_blocks", "pa_bm_refcount",
@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode_multi_split_workspace_size.restype = ctypes.c_size_t
     lib.pa_decode_multi_split.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32,
                                           f32, i32, i32, P, ctypes.c_size_t, P]
+    lib.pa_cache_and_decode.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P, P, ctypes.POINTER(CacheDesc), P, i32, P,
+                                        f32, f32, i32, i32, P, ctypes.c_size_t, P]
     lib.pa_decode_split_noalloc.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32,
                                             f32, i32, i32, P]
     D = ctypes.POINTER(CacheDesc)
@@ -102,6 +104,7 @@ def _load() -> ctypes.CDLL:
     lib.pa_get_device_error.argtypes = []
     lib.pa_version.argtypes = []
     for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split", "pa_decode_multi_split",
+                 "pa_cache_and_decode",
                  "pa_decode_split_noalloc",
                  "pa_set_check_mode",
                  "pa_get_device_error", "pa_version"):
@@ -311,6 +314,51 @@ def decode_multi_split(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor
                                        int(partition_size), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(dev))
     _check("pa_decode_multi_split", rc)
+
+
+def cache_and_decode(out: torch.Tensor, q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                     slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float = 1.0,
+                     max_context_len: int = 0, partition_size: int = 0,
+                     workspace: Optional[torch.Tensor] = None) -> None:
+    """One launch doing reshape_and_cache of the new rows and the decode (one
+    pass, or split when partition_size > 0).  q/out [S, Hq, D] (one new token)
+    or [S, k, Hq, D]; key/value [S * k, Hkv, D]; slot_mapping [S * k]."""
+    _check_caches(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", (torch.float16, torch.bfloat16), None, dev)
+    if q.dim() not in (3, 4):
+        raise ValueError("q must have 3 or 4 dims")
+    _need(out, "out", q.dtype, q.dim(), dev)
+    _need(key, "key", q.dtype, 3, dev)
+    _need(value, "value", q.dtype, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S = q.shape[0]
+    k = q.shape[1] if q.dim() == 4 else 1
+    Hq, D = q.shape[-2], q.shape[-1]
+    if out.shape != q.shape or block_tables.shape[0] != S or context_lens.shape[0] != S or D != k_cache.shape[3]:
+        raise ValueError("q/out/block_tables/context_lens shapes disagree")
+    if key.shape != value.shape or key.shape[0] != S * k or slot_mapping.shape[0] != S * k:
+        raise ValueError("key/value/slot_mapping must have num_seqs * num_q_tokens rows")
+    if key.shape[1] != k_cache.shape[1] or key.shape[2] != D:
+        raise ValueError("key rows do not match the cache's heads/head_dim")
+    ws_ptr, ws_bytes = None, 0
+    if partition_size > 0:
+        need = decode_multi_split_workspace_size(S, k, Hq, D, max_context_len, partition_size)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", device=dev)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        rc = lib.pa_cache_and_decode(_ptr(out), _ptr(q), _dtype_code(q.dtype), S, k, Hq, _ptr(key), _ptr(value),
+                                     _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+                                     _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale),
+                                     float(kv_scale), int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+                                     _stream(dev))
+    _check("pa_cache_and_decode", rc)
 
 
 def set_check_mode(enable: bool) -> bool:

@@ -52,7 +52,7 @@ def test_full_size_workload(idx):
     assert torch.isfinite(out.float()).all()
     if wl.partition_size:
         b2 = DeviceBatch(wl, "cuda", partition_size=0)
-        out2 = b2.decode()
+        out2 = b2.step()
     else:
         b2 = DeviceBatch(wl, "cuda", partition_size=512)
         out2 = b2.step()
