@@ -21,7 +21,8 @@
  *    partition and merges the partial results by log-sum-exp; it must equal
  *    the unsplit result up to rounding.
  *  - The scatter writes each new token's K and V rows into the slot named by
- *    its slot id (blocks are "extended each decode step", same review, §6).
+ *    its slot id (a sequence's blocks grow by one token every decode step:
+ *    same review, §6).
  *    FP8 E4M3 caches store round-to-nearest-even(x / kv_scale), saturated to
  *    the largest finite E4M3 value, and are read back as code * kv_scale.
  *
