@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-flush", action="store_true",
+                    help="never flush L2 between steps (steady state; the shared-prefix workload reads from L2)")
     ap.add_argument("--separate", action="store_true",
                     help="time the scatter and the decode as two launches instead of pa_cache_and_decode")
     ap.add_argument("--no-clocks", action="store_true")
@@ -318,7 +320,7 @@ def run_ours(args, wl, world, rank, local, pg):
     alg_bytes = wl.algorithmic_bytes() + (wl.scatter_bytes() if fused else 0)
     flush = None
     unique_bytes = int(wl.notes.get("unique_blocks", 0)) * wl.Hkv * wl.bs * wl.D * 2 * W.ELEM_BYTES[wl.kv_dtype]
-    if unique_bytes < 4 * L2_BYTES:
+    if unique_bytes < 4 * L2_BYTES and not args.no_flush:
         flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
 
     for _ in range(max(3, args.warmup)):
@@ -394,7 +396,9 @@ def run_ours(args, wl, world, rank, local, pg):
                        "head_dim": wl.D, "block_size": wl.bs, "kv_dtype": wl.kv_dtype,
                        "context_tokens": int(wl.context_lens.sum()), "max_context": wl.max_context_len,
                        "kv_bytes_per_step": kv_bytes, "partition_size": P,
-                       "l2": "inputs larger than L2" if flush is None else "256 MiB L2 flush between steps",
+                       "l2": ("256 MiB L2 flush between steps" if flush is not None else
+                              "no flush (steady state)" if args.no_flush and unique_bytes < 4 * L2_BYTES else
+                              "inputs larger than L2"),
                        "parallelism": "replicas" if world > 1 else "single",
                        "step": ("pa_cache_and_decode: scatter fused into the decode launch" if fused
                                 else "pa_reshape_and_cache, then the decode call")},
@@ -402,7 +406,9 @@ def run_ours(args, wl, world, rank, local, pg):
             "pct_of_hbm_peak": 100.0 * value / peak,
             "decode_kernel_us": 1e3 * dec_avg,
             "decode_kernel_us_median": 1e3 * statistics.median(dec_ms),
+            "decode_kernel_us_p10_p90": [1e3 * pct(dec_ms, 10), 1e3 * pct(dec_ms, 90)],
             "scatter_us": None if sc_ms is None else 1e3 * sum(sc_ms) / K,
+            "scatter_gbs": None if sc_ms is None else wl.scatter_bytes() / (sum(sc_ms) / K * 1e-3) / 1e9,
             "wall_s": wall,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
@@ -413,6 +419,12 @@ def run_ours(args, wl, world, rank, local, pg):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def pct(xs, q):
+    """q-th percentile (nearest rank) of a list."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q / 100.0 * (len(ys) - 1)))))]
 
 
 def e2e_measure(b, wl, dev, K, warm, pg):
