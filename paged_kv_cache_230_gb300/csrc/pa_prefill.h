@@ -10,7 +10,7 @@ namespace pa {
 constexpr int kPfRows = 128;     // query rows per CTA (MMA M, TMEM lanes)
 constexpr int kPfTile = 128;     // KV tokens per tile (MMA N of S, K of P.V)
 constexpr int kPfStages = 2;     // K/V tiles in flight
-constexpr int kPfThreads = 224;  // 4 softmax warps, K TMA warp, MMA warp, V TMA warp
+constexpr int kPfThreads = 384;  // softmax, epilogue and TMA/MMA warpgroups
 
 struct PrefillParams {
   void* out;                    // [S, C, Hq, 128] of the cache dtype
