@@ -237,12 +237,13 @@ def recorded_traffic(workload: str, kernel: str):
 # CPU oracle timing (the reference arm and the cpu_baseline object)
 # --------------------------------------------------------------------------
 
-def oracle_sample_time(wl: W.Workload, budget_s: float = 20.0):
-    """Times the oracle (scatter + decode, all host threads) on a bounded sample
-    of the batch: whole sequences in order until about `budget_s` of wall time
-    has been spent; returns (seconds, kv_bytes, seqs, threads)."""
+def oracle_sample_time(wl: W.Workload, budget_s: float = 20.0, threads: int = 0):
+    """Times the oracle (scatter + decode, on `threads` host threads, 0 = all)
+    on a bounded sample of the batch: whole sequences in order until about
+    `budget_s` of wall time has been spent; returns (seconds, kv_bytes, seqs,
+    threads)."""
     import oracle
-    threads = oracle.max_threads()
+    threads = threads if threads > 0 else oracle.max_threads()
     if wl.kv_dtype == W.FP8:
         kc = np.zeros(wl.cache_shape(), np.uint8)
         vc = np.zeros(wl.cache_shape(), np.uint8)
@@ -381,9 +382,12 @@ def run_ours(args, wl, world, rank, local, pg):
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         t, byts, nseq, threads = oracle_sample_time(wl, budget_s=10.0)
+        t1, byts1, nseq1, _ = oracle_sample_time(wl, budget_s=3.0, threads=1)
         cpu = {"value": byts / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": "fp64 C oracle (scatter + decode) over %d sequences of the same %d-sequence batch, in "
-                         "order with wrap-around (%.2f GB of KV), %.1f s" % (nseq, wl.S, byts / 1e9, t)}
+                         "order with wrap-around (%.2f GB of KV), %.1f s" % (nseq, wl.S, byts / 1e9, t),
+               "single_thread": {"value": byts1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                                 "sample": "%d sequences, %.2f GB of KV, %.1f s" % (nseq1, byts1 / 1e9, t1)}}
 
     if rank == 0:
         line = {
