@@ -413,8 +413,10 @@ int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t part
   p.Pmax = static_cast<int>(np);
   p.parts_per_cta = parts_per_cta(a.num_seqs, cache->num_kv_heads, p.Pmax);
   const size_t rows = static_cast<size_t>(a.num_seqs) * a.qlen * a.num_q_heads * np;
-  p.ws_ml = static_cast<float*>(workspace);
-  p.ws_o = p.ws_ml + rows * 2;
+  // partial outputs first: their rows of head_dim floats keep the 16-byte
+  // alignment of the workspace for the merge's vector loads
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_ml = p.ws_o + rows * cache->head_dim;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st);
   if (e == cudaSuccess) e = pa::launch_lse_merge(p, cache->head_dim, st);

@@ -958,73 +958,6 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
   }
 }
 
-// Log-sum-exp merge of the split partials of one (sequence, query head) per
-// CTA of 256 threads (one partial per run of partitions):  M = max_p m_p,  w_p = 2^(m_p - M),  L = sum_p l_p w_p,
-// out = sum_p w_p o_p / L.  The partitions are spread over the threads (the
-// partials are read with independent loads), and every sum is reduced in a
-// fixed order, so the result is deterministic.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeMaxParts = 4096;  // weights kept in shared memory; beyond, recomputed
-
-__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float u = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = is_max ? fmaxf(v, u) : v + u;
-  }
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-  __syncthreads();
-  return r;
-}
-
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodeParams p) {
-  constexpr int NGRP = kMergeThreads / D;  // partition groups
-  __shared__ float wsh[kMergeMaxParts];
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float acc_sh[NGRP][D];
-  const int row = blockIdx.x;  // (s * qlen + new token) * Hq + query head
-  const int s = row / (p.Hq * p.qlen);
-  const int lmax = min(p.maxB * p.bs, p.Pmax * p.partition_size);
-  const int L = min(max(p.context_lens[s], 0), lmax);
-  const int nparts = (L + p.partition_size - 1) / p.partition_size;
-  const int np = (nparts + p.parts_per_cta - 1) / p.parts_per_cta;  // runs, one partial each
-  if (np <= 1) return;  // written directly by the CTA that held every partition
-  const int tid = threadIdx.x;
-  const float* ml = p.ws_ml + static_cast<int64_t>(row) * p.Pmax * 2;
-  const float* o = p.ws_o + static_cast<int64_t>(row) * p.Pmax * D;
-  float mx = -CUDART_INF_F;
-  for (int i = tid; i < np; i += kMergeThreads) mx = fmaxf(mx, ml[2 * i]);
-  const float M = block_reduce(mx, red, true);
-  float lpart = 0.f;
-  for (int i = tid; i < np; i += kMergeThreads) {
-    const float w = ex2(ml[2 * i] - M);
-    if (i < kMergeMaxParts) wsh[i] = w;
-    lpart += ml[2 * i + 1] * w;
-  }
-  const float lsum = block_reduce(lpart, red, false);  // ends with a barrier: wsh is visible
-  const int grp = tid / D, d = tid % D;
-  float acc = 0.f;
-#pragma unroll 8
-  for (int i = grp; i < np; i += NGRP) {
-    const float w = i < kMergeMaxParts ? wsh[i] : ex2(ml[2 * i] - M);
-    acc += o[static_cast<int64_t>(i) * D + d] * w;
-  }
-  acc_sh[grp][d] = acc;
-  __syncthreads();
-  if (grp == 0) {
-    float total = acc_sh[0][d];
-#pragma unroll
-    for (int g = 1; g < NGRP; ++g) total += acc_sh[g][d];
-    store_out(p.out, static_cast<int64_t>(row) * D + d, p.q_dtype, lsum > 0.f ? total / lsum : 0.f);
-  }
-}
-
 // Ring stages: as many as fit when the variant's CTAs per SM (its register
 // budget) share the SM's shared memory, between 2 and 8.  More stages keep
 // more loads in flight per SM, which the two-CTA variants need to stay near
