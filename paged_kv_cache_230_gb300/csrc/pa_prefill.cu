@@ -35,7 +35,7 @@
 //           done, O / l from TMEM to the output, then the O buffer is free.
 // The softmax warpgroup takes 240 registers a thread, the epilogue 112 and
 // the TMA/MMA warpgroup 80 (setmaxnreg; 128 x 432 = 55296 of the 384 x 168 =
-// 64512 the CTA is launched with).
+// 64512 the CTA is launched with, which the launcher checks).
 // Every mbarrier wait gives up after about one second (error bit set); a
 // warp that gives up raises a shared abort flag that stops the others after
 // their current wait, and in-flight MMAs and TMA loads are drained (bounded)
@@ -76,6 +76,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// registers a thread of each warpgroup holds after setmaxnreg
+constexpr int kRegsSoftmax = 240, kRegsEpilogue = 112, kRegsTmaMma = 80;
 
 // Paired fp32 arithmetic: two lanes of one 64-bit register per FMA/ADD issue,
 // and a three-input max, halve the instruction count of the row softmax.
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // warpgroup executes the same setmaxnreg; the three shares sum to less than
   // the launch's total, so the increase never waits).
   if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" :: "n"(kRegsTmaMma) : "memory");
   if (warp == kKWarp || warp == kVWarp) {
     // ===================== TMA producers: q + K, V =====================
     const bool is_k = warp == kKWarp;
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }  // warp 11: idle
   } else if (warp < 4) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 240;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" :: "n"(kRegsSoftmax) : "memory");
     // ====================== softmax: one thread per row ======================
     const int r = tid;  // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     if (!ok) fail();
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" :: "n"(kRegsEpilogue) : "memory");
     // ====================== epilogue: one thread per row ======================
     const int qq = warp & 3;
     const int r = qq * 32 + lane;  // query row = TMEM lane
@@ -575,6 +577,17 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
                            const CUtensorMap& tmV, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  // the warpgroups' setmaxnreg shares must fit in the registers the CTA is
+  // launched with, or the softmax warps' increase would never be granted
+  static int launch_regs = 0;
+  if (launch_regs == 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, prefill_kernel);
+    if (e != cudaSuccess) return e;
+    launch_regs = fa.numRegs;
+  }
+  if (128 * (kRegsSoftmax + kRegsEpilogue + kRegsTmaMma) > launch_regs * kPfThreads)
+    return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the kernel holds all of an SM's tensor
   // memory), each walking the work items with a stride of the grid
   static int sms[64] = {0};
