@@ -201,36 +201,53 @@ DECODE_SOURCES = ("pa_decode.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_decode_f16
                   "pa_decode_fp8.cu")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources the decode kernel is compiled from."""
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
+
+
+def kernel_source_hash(sources=DECODE_SOURCES) -> str:
+    """Hash of the sources a kernel is compiled from (the decode kernel's by default)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_230_gb300", "csrc")
-    for name in DECODE_SOURCES:
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch recorded by an ncu capture under profiles/, valid
-    only while the kernel sources hash to the value recorded with it."""
-    path = os.path.join(ROOT, "profiles", "%s_%s.txt" % (kernel, workload))
+def _profile_values(name: str, sources) -> dict:
+    """The key: value lines of profiles/<name>.txt, or {} when the file is
+    missing or was captured from other kernel sources than the current ones."""
     try:
-        text = open(path).read()
+        text = open(os.path.join(ROOT, "profiles", name + ".txt")).read()
     except OSError:
-        return None
+        return {}
     vals = {}
     for ln in text.splitlines():
         if ":" in ln:
             k, v = ln.split(":", 1)
             v = v.split()
             vals[k.strip()] = v[0] if v else ""
-    if vals.get("kernel_source_hash") != kernel_source_hash():
-        return None
+    return vals if vals.get("kernel_source_hash") == kernel_source_hash(sources) else {}
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, valid
+    only while the kernel sources hash to the value recorded with it."""
     try:
-        return float(vals["dram_bytes_per_launch_full_size"])
+        return float(_profile_values("%s_%s" % (kernel, workload), DECODE_SOURCES)["dram_bytes_per_launch_full_size"])
     except (KeyError, ValueError):
         return None
+
+
+def recorded_prefill_traffic(chunk: int, seqs: int):
+    """DRAM bytes of one prefill launch over `seqs` sequences with a `chunk`-token
+    chunk at context 2 x chunk: the captured bytes per sequence (every
+    sequence reads its own q, K and V and writes its own output) times seqs."""
+    try:
+        per_seq = float(_profile_values("prefill_gqa8b_chunk%d" % chunk, PREFILL_SOURCES)["dram_bytes_per_sequence"])
+    except (KeyError, ValueError):
+        return None
+    return per_seq * seqs
 
 
 # --------------------------------------------------------------------------
@@ -599,7 +616,7 @@ def run_prefill(args, local):
         run()
     torch.cuda.synchronize()
     # time enough launches to fill about two seconds, so that the clock
-    # sampler (100 ms period) sees the kernel under load
+    # sampler sees the kernel under load for many periods
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(3):
@@ -636,7 +653,7 @@ def run_prefill(args, local):
             "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6), "clocks": clocks,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "peak_source": kind, "frac_of_burst_peak": tflops / burst,
-                         "kernel": "pa_prefill"}}
+                         "traffic": recorded_prefill_traffic(C, S), "kernel": "pa_prefill"}}
     print(json.dumps(line), flush=True)
 
 
