@@ -338,6 +338,18 @@ PA_API int pa_set_check_mode(int enable);
  */
 PA_API int pa_get_device_error(void);
 
+/*
+ * pa_selftest_wait_timeout: self-test of the bounded waits in the decode and
+ * prefill pipelines (every mbarrier wait there gives up after about one
+ * second instead of hanging).  Enqueues on `stream` one kernel whose thread
+ * waits, through the same wait helper, on a barrier that nothing arrives at:
+ * after about one second the wait gives up, the kernel records
+ * PA_DEVERR_TIMEOUT in the device error word and returns, and the context
+ * stays usable.  Returns PA_OK, or PA_ERR_CUDA if the launch fails; the bit
+ * shows in the next pa_get_device_error().
+ */
+PA_API int pa_selftest_wait_timeout(pa_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 PA_API int pa_version(void);
 

@@ -226,6 +226,11 @@ int64_t split_partitions(int32_t max_context_len, int32_t partition_size) {
 
 }  // namespace
 
+namespace pa {
+// pa_selftest.cu: one kernel whose bounded wait runs out
+cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t st);
+}  // namespace pa
+
 extern "C" {
 
 int pa_reshape_and_cache(const void* key, const void* value, int32_t in_dtype, int32_t num_tokens, void* k_cache,
@@ -556,6 +561,13 @@ int pa_set_check_mode(int enable) {
 }
 
 int pa_get_device_error(void) { return read_and_clear_error(nullptr, true); }
+
+int pa_selftest_wait_timeout(pa_stream_t stream) {
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return pa::launch_wait_timeout_selftest(err, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 int pa_version(void) { return 100; }
 

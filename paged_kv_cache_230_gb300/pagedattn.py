@@ -36,7 +36,7 @@ EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
            "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_num_free_blocks", "pa_bm_refcount",
            "pa_bm_tail_waste", "pa_bm_check", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
-           "pa_version"]
+           "pa_selftest_wait_timeout", "pa_version"]
 
 
 class PagedAttnError(RuntimeError):
@@ -102,12 +102,13 @@ def _load() -> ctypes.CDLL:
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_set_check_mode.argtypes = [ctypes.c_int]
     lib.pa_get_device_error.argtypes = []
+    lib.pa_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
     lib.pa_version.argtypes = []
     for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split", "pa_decode_multi_split",
                  "pa_cache_and_decode",
                  "pa_decode_split_noalloc",
                  "pa_set_check_mode",
-                 "pa_get_device_error", "pa_version"):
+                 "pa_get_device_error", "pa_selftest_wait_timeout", "pa_version"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -363,6 +364,14 @@ def cache_and_decode(out: torch.Tensor, q: torch.Tensor, key: torch.Tensor, valu
 
 def set_check_mode(enable: bool) -> bool:
     return bool(lib.pa_set_check_mode(1 if enable else 0))
+
+
+def selftest_wait_timeout() -> None:
+    """Enqueue, on torch's current stream, a kernel whose bounded mbarrier
+    wait runs out (nothing arrives): after about one second it records
+    DEVERR_TIMEOUT in the device error word and returns (read it with
+    get_device_error())."""
+    _check("pa_selftest_wait_timeout", lib.pa_selftest_wait_timeout(_stream(torch.device("cuda", torch.cuda.current_device()))))
 
 
 def get_device_error() -> int:
