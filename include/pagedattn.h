@@ -145,8 +145,10 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * num_q_tokens new tokens per sequence (positions L - C .. L - 1 of each
  * context; chunked prefill, review §10 table), computed on the tensor cores
  * with tcgen05 MMAs and tensor-memory accumulators for long chunks: prefill is
- * the compute-bound phase (review §7).  One CTA per (sequence, query head,
- * 128 query tokens) streams 128-token K/V tiles through the block table.
+ * the compute-bound phase (review §7).  The work items are (sequence, query
+ * head, 128 query tokens); the kernel is persistent, one CTA per SM walking
+ * the items, and streams each item's 128-token K/V tiles through the block
+ * table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, 128] of q_dtype
  * Supported: head_dim 128, 16-bit caches of the q dtype, block size 8, 16 or
  * 32, scale > 0.  Other arguments as pa_decode (no kv_scale: 16-bit caches

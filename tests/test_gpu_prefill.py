@@ -41,6 +41,26 @@ def test_prefill_matches_oracle(case):
             assert torch.all(out[s, j] == 0)
 
 
+def _draw(i):
+    rng = np.random.default_rng(3000 + i)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.integers(1, 7))
+    S = int(rng.integers(1, 4))
+    C = int(rng.integers(1, 401))
+    lens = [int(C + x) for x in rng.integers(0, 900, size=S)]
+    return (G * Hkv, Hkv, ["f16", "bf16"][int(rng.integers(0, 2))], int(rng.choice([8, 16, 32])), C, lens)
+
+
+SWEEP = [_draw(i) for i in range(12)]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: "Hq%d-Hkv%d-%s-bs%d-C%d" % c[:5])
+def test_prefill_sweep_matches_oracle(case):
+    """Seeded draws of group size, heads, dtype, block size, chunk length
+    (ragged against the 128-row tiles) and contexts."""
+    test_prefill_matches_oracle(case)
+
+
 def _prefill(g, wl, bt=None, kc=None, vc=None, cl=None):
     out = torch.full_like(g.q, float("nan"))
     _gpu.lib().prefill(out, g.q, g.kc if kc is None else kc, g.vc if vc is None else vc,
