@@ -169,11 +169,13 @@ PA_API size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_hea
 
 /*
  * pa_decode_split: the same result as pa_decode, computed per partition of
- * partition_size tokens (a multiple of 64) by separate CTAs; each writes its
- * unnormalised partial (o_p, m_p, l_p) to the workspace and a second kernel
- * merges them by log-sum-exp:  M = max_p m_p,  L = sum_p l_p 2^(m_p - M),
- * out = sum_p o_p 2^(m_p - M) / L  (scores kept in base 2).  Sequences with a
- * single partition are written directly.
+ * partition_size tokens (a multiple of 64): a CTA streams a run of
+ * consecutive partitions of one (sequence, kv head), folds their partials
+ * (o_p, m_p, l_p) by log-sum-exp in partition order and writes one
+ * unnormalised partial per run to the workspace; a second kernel merges the
+ * runs the same way:  M = max_p m_p,  L = sum_p l_p 2^(m_p - M),
+ * out = sum_p o_p 2^(m_p - M) / L  (scores kept in base 2).  Sequences held
+ * by a single run are written directly.
  *   max_context_len  >= every context_lens[s] (the host's own bound; longer
  *                    contexts are clamped and flagged)
  *   workspace        device buffer of at least workspace_bytes =
