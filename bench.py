@@ -286,6 +286,25 @@ def oracle_sample_time(wl: W.Workload, budget_s: float = 20.0, threads: int = 0)
     return total_t, total_b, nseq, threads
 
 
+def unique_kv_bytes(wl: W.Workload) -> int:
+    """KV bytes of the distinct physical blocks the batch reads."""
+    return int(wl.notes.get("unique_blocks", 0)) * wl.Hkv * wl.bs * wl.D * 2 * W.ELEM_BYTES[wl.kv_dtype]
+
+
+def workload_config(wl: W.Workload, P: int, world: int, fused: bool, no_flush: bool) -> dict:
+    """The `config` object of a decode bench line, the same for both arms."""
+    small = unique_kv_bytes(wl) < 4 * L2_BYTES
+    return {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
+            "head_dim": wl.D, "block_size": wl.bs, "kv_dtype": wl.kv_dtype, "new_tokens_per_seq": wl.qlen,
+            "context_tokens": int(wl.context_lens.sum()), "max_context": wl.max_context_len,
+            "kv_bytes_per_step": wl.kv_bytes(), "partition_size": P,
+            "l2": ("no flush (steady state)" if small and no_flush else
+                   "256 MiB L2 flush between steps" if small else "inputs larger than L2"),
+            "parallelism": "replicas" if world > 1 else "single",
+            "step": ("pa_cache_and_decode: scatter fused into the decode launch" if fused
+                     else "pa_reshape_and_cache, then the decode call")}
+
+
 def run_reference(args, wl, world, rank, pg):
     if rank != 0:
         return
@@ -305,8 +324,8 @@ def run_reference(args, wl, world, rank, pg):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * secs / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
-                   "head_dim": wl.D, "block_size": wl.bs, "kv_dtype": wl.kv_dtype},
+        "config": workload_config(wl, wl.partition_size if args.split < 0 else args.split, world,
+                                  not args.separate, args.no_flush),
         "decode_tokens_per_s": nseq / secs,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": "fp64 C oracle (scatter + decode) over leading sequences of the batch, "
@@ -337,8 +356,7 @@ def run_ours(args, wl, world, rank, local, pg):
     # the fused kernel also reads the new rows and writes them into the pool
     alg_bytes = wl.algorithmic_bytes() + (wl.scatter_bytes() if fused else 0)
     flush = None
-    unique_bytes = int(wl.notes.get("unique_blocks", 0)) * wl.Hkv * wl.bs * wl.D * 2 * W.ELEM_BYTES[wl.kv_dtype]
-    if unique_bytes < 4 * L2_BYTES and not args.no_flush:
+    if unique_kv_bytes(wl) < 4 * L2_BYTES and not args.no_flush:
         flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
 
     for _ in range(max(3, args.warmup)):
@@ -413,16 +431,7 @@ def run_ours(args, wl, world, rank, local, pg):
             "dtype": "bf16" if wl.q_dtype == "bf16" and wl.kv_dtype != W.FP8 else
                      ("e4m3-kv/bf16" if wl.kv_dtype == W.FP8 else "f16"),
             "data": "synthetic",
-            "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
-                       "head_dim": wl.D, "block_size": wl.bs, "kv_dtype": wl.kv_dtype,
-                       "context_tokens": int(wl.context_lens.sum()), "max_context": wl.max_context_len,
-                       "kv_bytes_per_step": kv_bytes, "partition_size": P,
-                       "l2": ("256 MiB L2 flush between steps" if flush is not None else
-                              "no flush (steady state)" if args.no_flush and unique_bytes < 4 * L2_BYTES else
-                              "inputs larger than L2"),
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "step": ("pa_cache_and_decode: scatter fused into the decode launch" if fused
-                                else "pa_reshape_and_cache, then the decode call")},
+            "config": workload_config(wl, P, world, fused, args.no_flush),
             "decode_tokens_per_s": seqs / (ms_per_step * 1e-3),
             "pct_of_hbm_peak": 100.0 * value / peak,
             "decode_kernel_us": 1e3 * dec_avg,

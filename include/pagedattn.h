@@ -161,7 +161,9 @@ PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seq
 
 /*
  * Workspace bytes pa_decode_split needs: num_seqs * num_q_heads *
- * ceil(max_context_len / partition_size) * (head_dim + 2) * 4.  Returns 0 for
+ * ceil(max_context_len / partition_size) * (head_dim + 2) * 4 (one fp32
+ * partial output row plus its (m, l) per partition of each query head; the
+ * partition and merge scheme is described at pa_decode_split).  Returns 0 for
  * invalid sizes.
  */
 PA_API size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -169,7 +171,14 @@ PA_API size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_hea
 
 /*
  * pa_decode_split: the same result as pa_decode, computed per partition of
- * partition_size tokens (a multiple of 64): a CTA streams a run of
+ * partition_size tokens (a multiple of 64).  The review's implementation
+ * cross-reference (§15, "Paged Attention Kernels": paged attention v1/v2)
+ * names a second paged-attention kernel beside the single-pass one without
+ * describing it; the pages give no partitioning or merge rule, so the
+ * partitions, their partial softmax states and the log-sum-exp merge below
+ * are this library's reading of that split-context kernel, chosen so that
+ * long contexts spread over many CTAs (decode is bandwidth bound, review
+ * §7).  A CTA streams a run of
  * consecutive partitions of one (sequence, kv head), folds their partials
  * (o_p, m_p, l_p) by log-sum-exp in partition order and writes one
  * unnormalised partial per run to the workspace; a second kernel merges the
@@ -231,7 +240,12 @@ PA_API int pa_decode_multi_split(void *out, const void *q, int32_t q_dtype, int3
  *                 position's slot in the sequence's own block table (a block
  *                 private to the sequence, as copy-on-write makes it); a slot
  *                 outside the pool is skipped, and either case sets
- *                 PA_DEVERR_SLOT.
+ *                 PA_DEVERR_SLOT.  In check mode a separate kernel first
+ *                 scans the live table entries of every other sequence of
+ *                 the batch and sets PA_DEVERR_SLOT when one of them names
+ *                 the block a new row goes to (copy-on-write skipped: the
+ *                 block is shared, so another sequence may read it while it
+ *                 is written); the row is still written.
  * Other arguments as pa_decode_multi / pa_decode_multi_split (workspace and
  * max_context_len are read only when partition_size > 0).
  */
@@ -250,12 +264,14 @@ PA_API int pa_cache_and_decode(void *out, const void *q, int32_t q_dtype, int32_
  * host framework that owns every device allocation of its plug-ins).  The
  * pages describe no such call; it exists only for those callers.
  * The partial results go to a 32 MiB scratch array compiled into the library
- * (held on every device that loads it until the process exits).  Returns
- * PA_ERR_WORKSPACE when pa_decode_split_workspace_size(num_seqs, num_q_heads,
- * head_dim, max_context_len, partition_size) exceeds 32 MiB; otherwise the
- * same arguments, results and errors as pa_decode_split.  The first call on a
- * device looks up the scratch address (cudaGetSymbolAddress) and should come
- * before any stream capture.  All calls on a device share the scratch, so
+ * (held on every device that loads it until the process exits).  The
+ * arguments, results and errors are those of pa_decode_split given a 32 MiB
+ * workspace: argument errors first, then PA_ERR_WORKSPACE when
+ * pa_decode_split_workspace_size(num_seqs, num_q_heads, head_dim,
+ * max_context_len, partition_size) exceeds 32 MiB; an empty batch returns
+ * PA_OK.  The first call on a device (and the first after its context was
+ * destroyed and created anew) looks up the scratch address
+ * (cudaGetSymbolAddress) and should come before any stream capture.  All calls on a device share the scratch, so
  * calls that can overlap on the GPU (unordered streams) race; calls ordered
  * on one stream are safe.  Allocates nothing.
  */

@@ -202,16 +202,21 @@ cudaError_t launch_decode(const pa::DecodeParams& p, const CUtensorMap& tk, cons
 #ifndef PA_SPLIT_CTAS_PER_SLOT
 #define PA_SPLIT_CTAS_PER_SLOT 16
 #endif
-int parts_per_cta(int S, int Hkv, int Pmax) {
-  static int sms[kMaxDevices] = {0};
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
-  if (sms[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    sms[dev] = n;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  const int64_t target = int64_t(PA_SPLIT_CTAS_PER_SLOT) * sms[dev] * pa::kMinCtasPerSm;
+  return n;
+}
+
+int parts_per_cta(int S, int Hkv, int Pmax) {
+  const int64_t target = int64_t(PA_SPLIT_CTAS_PER_SLOT) * sm_count() * pa::kMinCtasPerSm;
   const int64_t total = int64_t(S) * Hkv * Pmax;
   int64_t ppc = (total + target - 1) / target;
   if (ppc < 1) ppc = 1;
@@ -456,6 +461,17 @@ int pa_cache_and_decode(void* out, const void* q, int32_t q_dtype, int32_t num_s
   if (num_seqs == 0) return PA_OK;
   if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value)) return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_seqs) * num_q_tokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (check_mode()) {
+    // a fused write into a block that another sequence's table also names
+    // (copy-on-write skipped) would race with that sequence's tile loads
+    int* err = device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (pa::launch_shared_slot_check(slot_mapping, block_tables, context_lens, num_seqs, num_q_tokens,
+                                     max_blocks_per_seq, cache->block_size, cache->num_blocks, err,
+                                     st) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
   const CacheWrite w{key, value, slot_mapping, k_cache, v_cache};
   if (partition_size > 0)
     return decode_split_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream, &w);

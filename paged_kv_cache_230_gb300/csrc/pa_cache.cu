@@ -42,7 +42,46 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheParam
   store_row_piece<TO_FP8>(u, which ? p.v_cache : p.k_cache, dst, p.in_dtype, p.kv_scale);
 }
 
+// Check mode of the fused cache write: the new row of token (s, j) goes to
+// block slot / bs, which must be private to sequence s (copy-on-write gives a
+// sequence its own copy of a shared block before it appends).  One CTA per
+// new token scans the live table entries of every other sequence; a match
+// means another sequence's CTA may read that block while it is written, and
+// sets the slot error bit.
+__global__ void __launch_bounds__(256)
+    shared_slot_check_kernel(const int64_t* __restrict__ slots, const int32_t* __restrict__ block_tables,
+                             const int32_t* __restrict__ context_lens, int S, int qlen, int maxB, int bs,
+                             int64_t num_blocks, int* err) {
+  const int64_t tok = blockIdx.x;
+  const int s = static_cast<int>(tok / qlen);
+  const int64_t slot = slots[tok];
+  if (slot < 0 || slot >= num_blocks * bs) return;  // padding, or reported by the write itself
+  const int blk = static_cast<int>(slot / bs);
+  for (int t = 0; t < S; ++t) {
+    if (t == s) continue;
+    const int L = min(max(context_lens[t], 0), maxB * bs);
+    const int nblk = (L + bs - 1) / bs;
+    const int32_t* row = block_tables + static_cast<int64_t>(t) * maxB;
+    bool hit = false;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) hit |= __ldg(row + j) == blk;
+    if (__syncthreads_or(hit)) {
+      if (threadIdx.x == 0) atomicOr(err, kErrSlot);
+      return;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_shared_slot_check(const int64_t* slots, const int32_t* block_tables, const int32_t* context_lens,
+                                     int S, int qlen, int maxB, int bs, int64_t num_blocks, int* err,
+                                     cudaStream_t st) {
+  const int64_t tokens = static_cast<int64_t>(S) * qlen;
+  if (tokens == 0) return cudaSuccess;
+  shared_slot_check_kernel<<<static_cast<unsigned>(tokens), 256, 0, st>>>(slots, block_tables, context_lens, S,
+                                                                          qlen, maxB, bs, num_blocks, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const CacheParams& p, cudaStream_t st) {
   const int64_t total = static_cast<int64_t>(p.T) * p.Hkv * 2 * (p.D / 8);

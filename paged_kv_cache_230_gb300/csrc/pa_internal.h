@@ -77,6 +77,12 @@ struct CacheParams {
 
 cudaError_t launch_reshape_and_cache(const CacheParams& p, cudaStream_t st);
 
+// Check mode of pa_cache_and_decode: flags (PA_DEVERR_SLOT) a new row whose
+// block is also named by a live table entry of another sequence of the batch.
+cudaError_t launch_shared_slot_check(const int64_t* slots, const int32_t* block_tables, const int32_t* context_lens,
+                                     int S, int qlen, int maxB, int bs, int64_t num_blocks, int* err,
+                                     cudaStream_t st);
+
 // Whole-block moves: op 0 copy (ids = [n][2] pairs), 1 gather into buf,
 // 2 scatter from buf.  block_bytes is one block of one cache (a multiple of 16).
 cudaError_t launch_block_op(int op, void* buf, void* k_cache, void* v_cache, const int64_t* ids, int n,

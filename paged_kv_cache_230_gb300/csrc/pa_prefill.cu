@@ -40,6 +40,8 @@
 // warp that gives up raises a shared abort flag that stops the others after
 // their current wait, and in-flight MMAs and TMA loads are drained (bounded)
 // before the CTA releases its tensor memory and exits.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -579,28 +581,30 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
   if (e != cudaSuccess) return e;
   // the warpgroups' setmaxnreg shares must fit in the registers the CTA is
   // launched with, or the softmax warps' increase would never be granted
-  static int launch_regs = 0;
-  if (launch_regs == 0) {
+  static std::atomic<int> launch_regs{0};
+  int regs = launch_regs.load(std::memory_order_relaxed);
+  if (regs == 0) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, prefill_kernel);
     if (e != cudaSuccess) return e;
-    launch_regs = fa.numRegs;
+    regs = fa.numRegs;
+    launch_regs.store(regs, std::memory_order_relaxed);
   }
-  if (128 * (kRegsSoftmax + kRegsEpilogue + kRegsTmaMma) > launch_regs * kPfThreads)
+  if (128 * (kRegsSoftmax + kRegsEpilogue + kRegsTmaMma) > regs * kPfThreads)
     return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the kernel holds all of an SM's tensor
   // memory), each walking the work items with a stride of the grid
-  static int sms[64] = {0};
+  static std::atomic<int> sms[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (sms[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    sms[dev] = n;
+  int nsm = sms[dev].load(std::memory_order_relaxed);
+  if (nsm == 0) {
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0) nsm = 148;
+    sms[dev].store(nsm, std::memory_order_relaxed);
   }
   const long long nqt = (p.C + kPfRows - 1) / kPfRows;
   const long long items = nqt * p.Hq * p.S;
-  const long long grid = items < sms[dev] ? items : sms[dev];
+  const long long grid = items < nsm ? items : nsm;
   prefill_kernel<<<static_cast<unsigned>(grid), kPfThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }

@@ -76,3 +76,37 @@ def test_slot_outside_the_sequences_table_is_flagged():
     # consistent slots: nothing flagged
     pa.cache_and_decode(out, g.q, g.key, g.value, g.slots, g.kc, g.vc, g.bt, g.cl, wl.scale)
     assert pa.get_device_error() == 0
+
+
+@pytest.mark.parametrize("P", [0, 64])
+def test_check_mode_flags_a_write_into_a_block_another_table_names(P):
+    """Copy-on-write skipped: sequence 1 shares sequence 0's first three
+    blocks, including the partially filled one that sequence 0's new row goes
+    to.  Without check mode the write goes through unreported (the slot is in
+    sequence 0's own table); check mode scans the other tables and reports it."""
+    pa = _gpu.lib()
+    wl = W.make_workload(name="t", seed=53, context_lens=[40, 50, 20], Hq=8, Hkv=2, D=128, bs=16, q_dtype="bf16",
+                         kv_dtype="bf16")
+    g = _gpu.OnGpu(wl)
+    out = torch.empty_like(g.q)
+    assert pa.get_device_error() == 0
+    prev = pa.set_check_mode(True)
+    try:
+        # private tables: nothing to report
+        pa.cache_and_decode(out, g.q, g.key, g.value, g.slots, g.kc, g.vc, g.bt, g.cl, wl.scale,
+                            max_context_len=wl.max_context_len, partition_size=P)
+        bt = g.bt.clone()
+        bt[1, :3] = bt[0, :3]  # blocks of tokens 0-47 of sequence 1 = sequence 0's blocks 0-2
+        slots = g.slots.clone()  # row 0 goes to position 39, in block bt[0, 2]
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.cache_and_decode(out, g.q, g.key, g.value, slots, g.kc, g.vc, bt, g.cl, wl.scale,
+                                max_context_len=wl.max_context_len, partition_size=P)
+        assert e.value.status == -5
+        # the shared block is not the new row's once sequence 1 keeps only the
+        # full blocks 0-1 in common (block 2 private again): nothing reported
+        bt[1, 2] = g.bt[1, 2]
+        pa.cache_and_decode(out, g.q, g.key, g.value, slots, g.kc, g.vc, bt, g.cl, wl.scale,
+                            max_context_len=wl.max_context_len, partition_size=P)
+    finally:
+        pa.set_check_mode(prev)
+    assert pa.get_device_error() == 0
