@@ -406,7 +406,9 @@ def run_ours(args, wl, world, rank, local, pg):
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
     kernel_name = ("decode_multi_split" if P else "decode_multi") if wl.qlen > 1 else ("decode_split" if P else "decode")
-    if fused:
+    if b.tensor_core_path():
+        kernel_name = "attn_tc_split" if P else "attn_tc"
+    elif fused:
         kernel_name = "cache_and_" + kernel_name
     traffic = recorded_traffic(wl.name, kernel_name)
 

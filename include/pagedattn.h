@@ -28,8 +28,14 @@
  *  - FP8 caches use OCP E4M3 with one per-tensor scale: stored =
  *    e4m3_rne_satfinite(x / kv_scale), read back as stored * kv_scale.  For
  *    16-bit caches kv_scale must be 1.
- *  - Supported: head_dim 64 or 128; block_size 8, 16 or 32; G from 1 to 16;
+ *  - Supported: head_dim 64 or 128; block_size 8, 16 or 32; G from 1 to 128;
  *    q/out dtype f16 or bf16; cache dtype equal to the q dtype or FP8 E4M3.
+ *  - Two kernels serve the decode calls.  When the G query heads of a kv head
+ *    times the new tokens per sequence make at most 16 query columns, a
+ *    warp-MMA kernel streams each (sequence, kv head) once per CTA.  Wider
+ *    groups go to the tensor-core kernel of pa_prefill (query rows packed as
+ *    token x head, tcgen05 MMAs with TMEM accumulators), which needs
+ *    scale > 0 and, for now, 16-bit caches (PA_ERR_UNSUPPORTED for FP8).
  *  - Errors are return codes (pa_status); nothing is thrown across the ABI.
  *    Arguments are checked on the host before anything is launched; a failed
  *    check launches nothing.  Index values in device arrays are not read by
@@ -78,6 +84,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_LEN 0x2 /* context length < 0 or above the table/partitions */
 #define PA_DEVERR_SLOT 0x4        /* slot id outside [0, num_blocks * block_size)     */
 #define PA_DEVERR_TIMEOUT 0x8     /* a pipeline wait ran out (about one second)       */
+#define PA_DEVERR_LAYOUT 0x10     /* a kernel found its shared memory misaligned and did nothing */
 
 typedef struct {
     int64_t num_blocks;   /* physical blocks in the pool (NB)                 */
@@ -132,8 +139,10 @@ PA_API int pa_decode(void *out, const void *q, int32_t q_dtype, int32_t num_seqs
  *   out[s][j][g] = sum_{i <= L-k+j} softmax_i(scale * q[s][j][g] . k_i) v_i
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
  * A token whose position is negative (k > L) gets a zero output.  The k
- * tokens of all G query heads of a kv head are served by one CTA as G * k
- * MMA columns, so G * k must be at most 16.  Other arguments as pa_decode.
+ * tokens of all G query heads of a kv head share each K/V tile loaded: as
+ * G * k columns of the warp-MMA kernel when G * k <= 16, as G * k rows of
+ * the tensor-core kernel otherwise (then scale > 0).  Other arguments as
+ * pa_decode.
  */
 PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                            int32_t num_q_heads, const void *k_cache, const void *v_cache,
@@ -144,15 +153,17 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * pa_prefill: the same causal attention as pa_decode_multi for a chunk of C =
  * num_q_tokens new tokens per sequence (positions L - C .. L - 1 of each
  * context; chunked prefill, review §10 table), computed on the tensor cores
- * with tcgen05 MMAs and tensor-memory accumulators for long chunks: prefill is
- * the compute-bound phase (review §7).  The work items are (sequence, query
- * head, 128 query tokens); the kernel is persistent, one CTA per SM walking
- * the items, and streams each item's 128-token K/V tiles through the block
- * table.
- *   out, q   [num_seqs, num_q_tokens, num_q_heads, 128] of q_dtype
- * Supported: head_dim 128, 16-bit caches of the q dtype, block size 8, 16 or
- * 32, scale > 0.  Other arguments as pa_decode (no kv_scale: 16-bit caches
- * only).
+ * with tcgen05 MMAs and tensor-memory accumulators: prefill is the
+ * compute-bound phase (review §7).  The queries of a (sequence, kv head) are
+ * packed as rows token * G + head, floor(128 / G) tokens x G heads per
+ * 128-row tile, so every K/V tile loaded serves all G heads; a work item
+ * holds two such tiles, whose MMAs alternate on the tensor core.  The kernel
+ * is persistent, one CTA per SM walking the items (longest contexts first),
+ * and streams each item's 128-token K/V tiles through the block table.
+ *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
+ * Supported: head_dim 64 or 128, 16-bit caches of the q dtype, block size 8,
+ * 16 or 32, G up to 128, scale > 0.  Other arguments as pa_decode (no
+ * kv_scale: 16-bit caches only).
  */
 PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                       int32_t num_q_heads, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,

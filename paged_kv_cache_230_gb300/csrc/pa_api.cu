@@ -7,8 +7,8 @@
 #include <mutex>
 
 #include "pagedattn.h"
+#include "pa_attn_tc.h"
 #include "pa_internal.h"
-#include "pa_prefill.h"
 
 namespace {
 
@@ -61,6 +61,7 @@ int finish(cudaError_t launch, cudaStream_t st) {
   if (!check_mode()) return PA_OK;
   const int bits = read_and_clear_error(st, false);
   if (bits < 0) return bits;
+  if (bits & PA_DEVERR_LAYOUT) return PA_ERR_CUDA;
   if (bits & PA_DEVERR_TIMEOUT) return PA_ERR_TIMEOUT;
   if (bits) return PA_ERR_BAD_INDEX;
   return PA_OK;
@@ -142,6 +143,11 @@ struct DecodeArgs {
   float scale, kv_scale;
 };
 
+// The group product of a (sequence, kv head) has G * qlen query columns; up
+// to kMaxGroup the warp-MMA decode kernel serves them, beyond that the
+// tensor-core kernel (query rows packed as token x head).
+bool use_tc(int G, int qlen) { return static_cast<int64_t>(G) * qlen > pa::kMaxGroup; }
+
 int check_decode(const DecodeArgs& a) {
   int rc = check_cache(a.cache, a.k_cache, a.v_cache);
   if (rc) return rc;
@@ -150,9 +156,14 @@ int check_decode(const DecodeArgs& a) {
   if (a.cache->kv_dtype != PA_FP8_E4M3 && a.cache->kv_dtype != a.q_dtype) return PA_ERR_UNSUPPORTED;
   if (a.num_q_heads % a.cache->num_kv_heads) return PA_ERR_INVALID_ARG;
   if (a.qlen < 1) return PA_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(a.num_q_heads / a.cache->num_kv_heads) * a.qlen > pa::kMaxGroup)
-    return PA_ERR_UNSUPPORTED;
+  const int G = a.num_q_heads / a.cache->num_kv_heads;
+  if (G > pa::kTcMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!std::isfinite(a.scale)) return PA_ERR_INVALID_ARG;
+  if (use_tc(G, a.qlen)) {
+    // the tensor-core path takes the row max of the raw scores
+    if (!(a.scale > 0.f)) return PA_ERR_INVALID_ARG;
+    if (a.cache->kv_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  }
   rc = check_kv_scale(a.cache->kv_dtype, a.kv_scale);
   if (rc) return rc;
   if (static_cast<int64_t>(a.max_blocks_per_seq) * a.cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
@@ -229,6 +240,148 @@ int64_t split_partitions(int32_t max_context_len, int32_t partition_size) {
   return (static_cast<int64_t>(max_context_len) + partition_size - 1) / partition_size;
 }
 
+// The new rows a fused call writes into the pool (pa_cache_and_decode).
+struct CacheWrite {
+  const void* key;
+  const void* value;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+};
+
+void set_cache_write(pa::DecodeParams& p, const CacheWrite* w) {
+  if (!w) return;
+  p.new_key = w->key;
+  p.new_value = w->value;
+  p.slot_mapping = w->slot_mapping;
+  p.k_cache = w->k_cache;
+  p.v_cache = w->v_cache;
+}
+
+// Consecutive partitions per run of the tensor-core kernel: about eight
+// work items per SM when every sequence has Pmax partitions (its CTAs are
+// persistent, so more items only cost per-item pipeline ramps).
+int tc_parts_per_run(int64_t units, int Pmax) {
+  const int64_t target = int64_t(8) * sm_count();
+  int64_t ppc = (units * Pmax + target - 1) / target;
+  if (ppc < 1) ppc = 1;
+  if (ppc > Pmax) ppc = Pmax;
+  return static_cast<int>(ppc);
+}
+
+// Attention of a.qlen new tokens per sequence on the tensor cores (chunked
+// prefill, and multi-token decode with a wide query group): causal among
+// the new tokens; split into runs of partitions merged by log-sum-exp when
+// partition_size > 0.  Arguments are checked by the caller.
+int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition_size, void* workspace,
+                 size_t workspace_bytes, pa_stream_t stream, const CacheWrite* write) {
+  const pa_cache_desc* cache = a.cache;
+  const int S = a.num_seqs, C = a.qlen, Hq = a.num_q_heads, Hkv = cache->num_kv_heads, D = cache->head_dim;
+  const int G = Hq / Hkv;
+  if (S == 0) return PA_OK;
+  const int T = std::min(C, pa::kTcRows / G);  // new tokens per query tile
+  const int64_t n_qt = (C + T - 1) / T;
+  const int NQ = n_qt >= 2 ? 2 : 1;
+  const int64_t n_qp = (n_qt + NQ - 1) / NQ;
+  int64_t Pmax = 1, ppc = 1, R = 1;
+  if (partition_size > 0) {
+    Pmax = split_partitions(max_context_len, partition_size);
+    if (Pmax > INT32_MAX) return PA_ERR_INVALID_ARG;
+    ppc = tc_parts_per_run(int64_t(S) * Hkv * n_qp, static_cast<int>(Pmax));
+    R = (Pmax + ppc - 1) / ppc;
+  }
+  const int64_t total = int64_t(S) * Hkv * n_qp * R;
+  const int64_t rows = int64_t(S) * C;
+  if (total > INT32_MAX || rows * Hq > INT32_MAX || rows > UINT32_MAX) return PA_ERR_INVALID_ARG;
+  if (partition_size > 0) {
+    const size_t need = pa_decode_multi_split_workspace_size(S, C, Hq, D, max_context_len, partition_size);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  }
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  int rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, a.k_cache, cache)) || (rc = make_cache_tensor_map(&tv, a.v_cache, cache)))
+    return rc;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  // q as {channels, heads, tokens}; box = 64 channels x the G heads of a kv
+  // head x T tokens, landing as rows token * G + head of 128 bytes
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hq), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(Hq) * D * 2};
+  const cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(T)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_CUDA;
+  pa::TcParams p{};
+  p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.err = err;
+  p.num_blocks = cache->num_blocks;
+  p.S = S;
+  p.C = C;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.bs = cache->block_size;
+  p.maxB = a.max_blocks_per_seq;
+  p.D = D;
+  p.T = T;
+  p.n_qt = static_cast<int>(n_qt);
+  p.NQ = NQ;
+  p.n_qp = static_cast<int>(n_qp);
+  p.R = static_cast<int>(R);
+  p.partition_size = partition_size > 0 ? partition_size : 0;
+  p.Pmax = static_cast<int>(Pmax);
+  p.ppc = static_cast<int>(ppc);
+  p.nslot = pa::tc_ring_slots(D, NQ);
+  p.rank_seqs = 1;
+  p.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+  p.total = static_cast<int>(total);
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  if (partition_size > 0) {
+    // partial outputs first (16-byte aligned rows for the merge), then (m, l)
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = p.ws_o + static_cast<size_t>(rows) * Hq * Pmax * D;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (write) {
+    // the new rows go to the pool first (the fused form of the warp-MMA path
+    // writes them from inside its decode kernel)
+    pa::CacheParams cp{};
+    cp.key = write->key;
+    cp.value = write->value;
+    cp.k_cache = write->k_cache;
+    cp.v_cache = write->v_cache;
+    cp.slot_mapping = write->slot_mapping;
+    cp.err = err;
+    cp.num_blocks = cache->num_blocks;
+    cp.T = static_cast<int>(rows);
+    cp.Hkv = Hkv;
+    cp.D = D;
+    cp.bs = cache->block_size;
+    cp.in_dtype = a.q_dtype;
+    cp.cache_dtype = cache->kv_dtype;
+    cp.kv_scale = 1.0f;
+    e = pa::launch_reshape_and_cache(cp, st);
+  }
+  if (e == cudaSuccess) e = pa::launch_attn_tc(p, tq, tk, tv, st);
+  if (e == cudaSuccess && partition_size > 0) {
+    pa::DecodeParams mp = make_params(a, err);
+    mp.partition_size = partition_size;
+    mp.Pmax = p.Pmax;
+    mp.parts_per_cta = p.ppc;
+    mp.ws_o = p.ws_o;
+    mp.ws_ml = p.ws_ml;
+    e = pa::launch_lse_merge(mp, D, st);
+  }
+  return finish(e, st);
+}
+
 }  // namespace
 
 namespace pa {
@@ -279,6 +432,7 @@ int pa_decode(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32
                      max_blocks_per_seq, context_lens, scale, kv_scale};
   int rc = check_decode(a);
   if (rc || num_seqs == 0) return rc;
+  if (use_tc(num_q_heads / cache->num_kv_heads, 1)) return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
   if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
   int* err = device_error_ptr();
   if (!err) return PA_ERR_CUDA;
@@ -298,6 +452,8 @@ int pa_decode_multi(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
   int rc = check_decode(a);
   if (rc || num_seqs == 0) return rc;
+  if (use_tc(num_q_heads / cache->num_kv_heads, num_q_tokens))
+    return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
   if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
   int* err = device_error_ptr();
   if (!err) return PA_ERR_CUDA;
@@ -317,48 +473,16 @@ int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int3
   if (rc) return rc;
   if (num_seqs < 0 || num_q_tokens < 1 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (cache->kv_dtype != q_dtype || cache->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
   if (num_q_heads % cache->num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (num_q_heads / cache->num_kv_heads > pa::kTcMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_blocks_per_seq) * cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !block_tables || !context_lens || !aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
-  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_tokens;
-  const int64_t nqt = (num_q_tokens + pa::kPfRows - 1) / pa::kPfRows;
-  if (rows > UINT32_MAX || nqt * num_q_heads * num_seqs > INT32_MAX) return PA_ERR_INVALID_ARG;
-  int* err = device_error_ptr();
-  if (!err) return PA_ERR_CUDA;
-  CUtensorMap tq, tk, tv;
-  if ((rc = make_cache_tensor_map(&tk, k_cache, cache)) || (rc = make_cache_tensor_map(&tv, v_cache, cache)))
-    return rc;
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return PA_ERR_CUDA;
-  // q as {128 channels, heads, tokens}; box = 64 channels x 1 head x 128 tokens
-  const cuuint64_t dims[3] = {128, cuuint64_t(num_q_heads), cuuint64_t(rows)};
-  const cuuint64_t strides[2] = {256, cuuint64_t(num_q_heads) * 256};
-  const cuuint32_t box[3] = {64, 1, cuuint32_t(pa::kPfRows)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return PA_ERR_CUDA;
-  pa::PrefillParams p{};
-  p.out = out;
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.err = err;
-  p.num_blocks = cache->num_blocks;
-  p.S = num_seqs;
-  p.C = num_q_tokens;
-  p.Hq = num_q_heads;
-  p.Hkv = cache->num_kv_heads;
-  p.G = num_q_heads / cache->num_kv_heads;
-  p.bs = cache->block_size;
-  p.maxB = max_blocks_per_seq;
-  p.bf16 = q_dtype == PA_BF16 ? 1 : 0;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return finish(pa::launch_prefill(p, tq, tk, tv, st), st);
+  const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, 1.0f};
+  return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
 }
 
 size_t pa_decode_multi_split_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
@@ -379,24 +503,6 @@ size_t pa_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
 
 namespace {
 
-// The new rows a fused call writes into the pool (pa_cache_and_decode).
-struct CacheWrite {
-  const void* key;
-  const void* value;
-  const int64_t* slot_mapping;
-  void* k_cache;
-  void* v_cache;
-};
-
-void set_cache_write(pa::DecodeParams& p, const CacheWrite* w) {
-  if (!w) return;
-  p.new_key = w->key;
-  p.new_value = w->value;
-  p.slot_mapping = w->slot_mapping;
-  p.k_cache = w->k_cache;
-  p.v_cache = w->v_cache;
-}
-
 // Split decode of one or several new tokens per sequence: the partition
 // kernel, then the log-sum-exp merge of the runs, on one stream.
 int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition_size, void* workspace,
@@ -405,6 +511,8 @@ int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t part
   if (rc) return rc;
   if (partition_size <= 0 || partition_size % pa::kTileTokens || max_context_len < 0) return PA_ERR_INVALID_ARG;
   if (a.num_seqs == 0) return PA_OK;
+  if (use_tc(a.num_q_heads / a.cache->num_kv_heads, a.qlen))
+    return attn_tc_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream, write);
   const pa_cache_desc* cache = a.cache;
   const int64_t np = split_partitions(max_context_len, partition_size);
   if (static_cast<int64_t>(a.num_seqs) * cache->num_kv_heads * np > INT32_MAX) return PA_ERR_INVALID_ARG;
@@ -475,6 +583,8 @@ int pa_cache_and_decode(void* out, const void* q, int32_t q_dtype, int32_t num_s
   const CacheWrite w{key, value, slot_mapping, k_cache, v_cache};
   if (partition_size > 0)
     return decode_split_impl(a, max_context_len, partition_size, workspace, workspace_bytes, stream, &w);
+  if (use_tc(num_q_heads / cache->num_kv_heads, num_q_tokens))
+    return attn_tc_impl(a, 0, 0, nullptr, 0, stream, &w);
   if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
   int* err = device_error_ptr();
   if (!err) return PA_ERR_CUDA;

@@ -103,7 +103,13 @@ class DeviceBatch:
                             self.partition_size, self.workspace)
         return self.out
 
+    def tensor_core_path(self) -> bool:
+        """Whether the decode goes to the tensor-core kernel (query group of
+        more than 16 columns) instead of the warp-MMA decode kernel."""
+        return self.wl.G * self.wl.qlen > 16
+
     def launches_per_step(self) -> int:
-        if self.fused:
-            return 2 if self.partition_size else 1
-        return 3 if self.partition_size else 2
+        merge = 1 if self.partition_size else 0
+        if self.fused and not self.tensor_core_path():
+            return 1 + merge  # the scatter runs inside the decode launch
+        return 2 + merge

@@ -29,7 +29,7 @@ PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: "workspace",
           -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out",
           -7: "not enough free blocks", -8: "unknown or duplicate sequence id"}
-DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_LAYOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill", "pa_decode_split_workspace_size",
            "pa_decode_split", "pa_decode_multi_split_workspace_size", "pa_decode_multi_split", "pa_cache_and_decode",
            "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
@@ -234,7 +234,7 @@ def decode_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
 
 def prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float) -> None:
-    """Chunked prefill on the tensor cores: q/out [S, C, Hq, 128], causal over the paged context."""
+    """Chunked prefill on the tensor cores: q/out [S, C, Hq, D] (D 64 or 128), causal over the paged context."""
     _check_caches(k_cache, v_cache)
     dev = k_cache.device
     _need(q, "q", (torch.float16, torch.bfloat16), 4, dev)

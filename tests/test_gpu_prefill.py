@@ -139,11 +139,11 @@ def test_single_new_token_and_empty_batch():
 
 def test_unsupported_and_invalid_arguments_launch_nothing():
     pa = _gpu.lib()
-    q = torch.zeros((1, 4, 2, 64), dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros((4, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
     bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
     cl = torch.full((1,), 4, dtype=torch.int32, device="cuda")
-    with pytest.raises(pa.PagedAttnError) as e:  # head_dim 64: the prefill kernel is built for 128
+    q = torch.zeros((1, 4, 2, 96), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((4, 2, 16, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:  # head_dim 96: not built
         pa.prefill(q.clone(), q, kc, kc, bt, cl, 0.1)
     assert e.value.status == -2
     q = torch.zeros((1, 4, 2, 128), dtype=torch.bfloat16, device="cuda")
