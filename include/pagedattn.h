@@ -35,7 +35,7 @@
  *    warp-MMA kernel streams each (sequence, kv head) once per CTA.  Wider
  *    groups go to the tensor-core kernel of pa_prefill (query rows packed as
  *    token x head, tcgen05 MMAs with TMEM accumulators), which needs
- *    scale > 0 and, for now, 16-bit caches (PA_ERR_UNSUPPORTED for FP8).
+ *    scale > 0.
  *  - Errors are return codes (pa_status); nothing is thrown across the ABI.
  *    Arguments are checked on the host before anything is launched; a failed
  *    check launches nothing.  Index values in device arrays are not read by
@@ -161,14 +161,17 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * is persistent, one CTA per SM walking the items (longest contexts first),
  * and streams each item's 128-token K/V tiles through the block table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
- * Supported: head_dim 64 or 128, 16-bit caches of the q dtype, block size 8,
- * 16 or 32, G up to 128, scale > 0.  Other arguments as pa_decode (no
- * kv_scale: 16-bit caches only).
+ * Supported: head_dim 64 or 128, caches of the q dtype or FP8 E4M3, block
+ * size 8, 16 or 32, G up to 128, scale > 0.  E4M3 tiles are widened exactly
+ * to f16 in shared memory and the MMAs run in f16; bf16 q is then scaled per
+ * query row by a power of two 2^e (max|q| 2^e in [2^14, 2^15)) and rounded
+ * to f16, exact but for entries below 2^-29 of the row's largest.  Other
+ * arguments as pa_decode (kv_scale must be 1 for 16-bit caches).
  */
 PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                       int32_t num_q_heads, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
-                      float scale, pa_stream_t stream);
+                      float scale, float kv_scale, pa_stream_t stream);
 
 /*
  * Workspace bytes pa_decode_split needs: num_seqs * num_q_heads *

@@ -9,6 +9,7 @@
 #include "pagedattn.h"
 #include "pa_attn_tc.h"
 #include "pa_internal.h"
+#include "pa_prefill.h"
 
 namespace {
 
@@ -159,11 +160,8 @@ int check_decode(const DecodeArgs& a) {
   const int G = a.num_q_heads / a.cache->num_kv_heads;
   if (G > pa::kTcMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!std::isfinite(a.scale)) return PA_ERR_INVALID_ARG;
-  if (use_tc(G, a.qlen)) {
-    // the tensor-core path takes the row max of the raw scores
-    if (!(a.scale > 0.f)) return PA_ERR_INVALID_ARG;
-    if (a.cache->kv_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
-  }
+  // the tensor-core path takes the row max of the raw scores
+  if (use_tc(G, a.qlen) && !(a.scale > 0.f)) return PA_ERR_INVALID_ARG;
   rc = check_kv_scale(a.cache->kv_dtype, a.kv_scale);
   if (rc) return rc;
   if (static_cast<int64_t>(a.max_blocks_per_seq) * a.cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
@@ -281,16 +279,15 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
   if (S == 0) return PA_OK;
   const int T = std::min(C, pa::kTcRows / G);  // new tokens per query tile
   const int64_t n_qt = (C + T - 1) / T;
-  const int NQ = n_qt >= 2 ? 2 : 1;
-  const int64_t n_qp = (n_qt + NQ - 1) / NQ;
+  const int fp8 = cache->kv_dtype == PA_FP8_E4M3 ? 1 : 0;
   int64_t Pmax = 1, ppc = 1, R = 1;
   if (partition_size > 0) {
     Pmax = split_partitions(max_context_len, partition_size);
     if (Pmax > INT32_MAX) return PA_ERR_INVALID_ARG;
-    ppc = tc_parts_per_run(int64_t(S) * Hkv * n_qp, static_cast<int>(Pmax));
+    ppc = tc_parts_per_run(int64_t(S) * Hkv * n_qt, static_cast<int>(Pmax));
     R = (Pmax + ppc - 1) / ppc;
   }
-  const int64_t total = int64_t(S) * Hkv * n_qp * R;
+  const int64_t total = int64_t(S) * Hkv * n_qt * R;
   const int64_t rows = int64_t(S) * C;
   if (total > INT32_MAX || rows * Hq > INT32_MAX || rows > UINT32_MAX) return PA_ERR_INVALID_ARG;
   if (partition_size > 0) {
@@ -331,17 +328,22 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
   p.D = D;
   p.T = T;
   p.n_qt = static_cast<int>(n_qt);
-  p.NQ = NQ;
-  p.n_qp = static_cast<int>(n_qp);
   p.R = static_cast<int>(R);
   p.partition_size = partition_size > 0 ? partition_size : 0;
   p.Pmax = static_cast<int>(Pmax);
   p.ppc = static_cast<int>(ppc);
-  p.nslot = pa::tc_ring_slots(D, NQ);
+  p.nslot = pa::tc_ring_slots(D, fp8);
   p.rank_seqs = 1;
-  p.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+  p.out_bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+  // E4M3 caches are widened to f16 (exact), so the MMA runs in f16; bf16 q
+  // is then scaled per row by a power of two and rounded to f16 in the kernel
+  p.fp8 = fp8;
+  p.bf16 = fp8 ? 0 : p.out_bf16;
+  p.q_scale_rows = fp8 && p.out_bf16 ? 1 : 0;
   p.total = static_cast<int>(total);
-  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  const double kvs = fp8 ? static_cast<double>(a.kv_scale) : 1.0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * kvs * 1.4426950408889634);
+  p.vscale = static_cast<float>(kvs);
   if (partition_size > 0) {
     // partial outputs first (16-byte aligned rows for the merge), then (m, l)
     p.ws_o = static_cast<float*>(workspace);
@@ -366,7 +368,7 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
     cp.bs = cache->block_size;
     cp.in_dtype = a.q_dtype;
     cp.cache_dtype = cache->kv_dtype;
-    cp.kv_scale = 1.0f;
+    cp.kv_scale = fp8 ? a.kv_scale : 1.0f;
     e = pa::launch_reshape_and_cache(cp, st);
   }
   if (e == cudaSuccess) e = pa::launch_attn_tc(p, tq, tk, tv, st);
@@ -380,6 +382,50 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
     e = pa::launch_lse_merge(mp, D, st);
   }
   return finish(e, st);
+}
+
+// Chunked prefill with 16-bit caches and head_dim 128 through the per-head
+// persistent kernel (pa_prefill.cu): work items (sequence, query head, 128
+// new tokens).  Arguments are checked by the caller.
+int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
+  const pa_cache_desc* cache = a.cache;
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.qlen;
+  const int64_t nqt = (a.qlen + pa::kPfRows - 1) / pa::kPfRows;
+  if (rows > UINT32_MAX || nqt * a.num_q_heads * a.num_seqs > INT32_MAX) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  int rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_cache_tensor_map(&tk, a.k_cache, cache)) || (rc = make_cache_tensor_map(&tv, a.v_cache, cache)))
+    return rc;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  // q as {128 channels, heads, tokens}; box = 64 channels x 1 head x 128 tokens
+  const cuuint64_t dims[3] = {128, cuuint64_t(a.num_q_heads), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {256, cuuint64_t(a.num_q_heads) * 256};
+  const cuuint32_t box[3] = {64, 1, cuuint32_t(pa::kPfRows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_CUDA;
+  pa::PrefillParams p{};
+  p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.err = err;
+  p.num_blocks = cache->num_blocks;
+  p.S = a.num_seqs;
+  p.C = a.qlen;
+  p.Hq = a.num_q_heads;
+  p.Hkv = cache->num_kv_heads;
+  p.G = a.num_q_heads / cache->num_kv_heads;
+  p.bs = cache->block_size;
+  p.maxB = a.max_blocks_per_seq;
+  p.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return finish(pa::launch_prefill(p, tq, tk, tv, st), st);
 }
 
 }  // namespace
@@ -468,20 +514,23 @@ int pa_decode_multi(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
 int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                int32_t num_q_heads, const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
                const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens, float scale,
-               pa_stream_t stream) {
+               float kv_scale, pa_stream_t stream) {
   int rc = check_cache(cache, k_cache, v_cache);
   if (rc) return rc;
   if (num_seqs < 0 || num_q_tokens < 1 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (cache->kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != q_dtype && cache->kv_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
   if (num_q_heads % cache->num_kv_heads) return PA_ERR_INVALID_ARG;
   if (num_q_heads / cache->num_kv_heads > pa::kTcMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+  rc = check_kv_scale(cache->kv_dtype, kv_scale);
+  if (rc) return rc;
   if (static_cast<int64_t>(max_blocks_per_seq) * cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !block_tables || !context_lens || !aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
   const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
-                     max_blocks_per_seq, context_lens, scale, 1.0f};
+                     max_blocks_per_seq, context_lens, scale, kv_scale};
+  if (cache->kv_dtype != PA_FP8_E4M3 && cache->head_dim == 128) return prefill_per_head_impl(a, stream);
   return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
 }
 

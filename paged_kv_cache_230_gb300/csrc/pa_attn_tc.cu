@@ -8,32 +8,37 @@
 // Rows.  The queries of one (sequence, kv head) are the pairs (new token j,
 // query head g of the kv head's group of G), packed as row = j * G + g, so a
 // 128-row query tile holds T = floor(128 / G) tokens of every head of the
-// group and each K/V tile loaded serves all of them (GQA reuse).  A work
-// item holds NQ = 2 consecutive query tiles when there are two (one
-// otherwise): both read the same K/V tiles, and their MMAs alternate
-// accumulators instruction by instruction, which is what keeps the tensor
-// core at full rate (a chain of MMAs into one accumulator waits on itself).
+// group and each K/V tile loaded serves all of them (GQA reuse).
 //
-// Persistent: one CTA per SM walks the work items c, c + grid, ...; the
-// items are ordered by context length, longest first, then by kv head, last
-// query tiles first (they attend to the most tokens), and runs of partitions
-// in the split variant.  16 warps in four warpgroups:
-//   warps 0-3, 4-7  softmax of query tile 0 and 1, one thread per row (=
-//       TMEM lane): tcgen05.ld of the 128 scores, causal mask where a tile
-//       crosses the row's position, online softmax in base 2 with a
-//       reference max that moves only by more than 2^8 (O rescaled in TMEM
-//       then), P written as 16-bit pairs to shared memory (the A operand of
-//       P.V);
-//   warps 8-11  epilogue, one thread per row: O / l from TMEM to the output
-//       (or the unnormalised partial and its (m, l) to the split workspace);
-//   warp 12     TMA: each item's query tiles, then its 128-token K and V
-//       tiles block by block through the block table into a ring of slots,
-//       in the order the tensor core consumes them;
-//   warp 13     one thread issues tcgen05.mma: S_i = Q_i K^T (both operands
-//       in shared memory) into TMEM, then O_i += P_i V once the softmax has
-//       written P_i.  The scores of tile t + 1 are computed while the
-//       softmax works on tile t: a score buffer is free as soon as its
-//       softmax has loaded it into registers.
+// Pipeline of one CTA (persistent: one per SM, walking the work items c,
+// c + grid, ...; items ordered by context length, longest first, then kv
+// head, last query tiles first, then runs of partitions in the split
+// variant).  Tensor memory holds two score buffers S (128 columns each), two
+// probability buffers P (64 columns each: 16-bit pairs) and the output O, so
+// the tensor core never waits on its own results: while the softmax works on
+// tile g, one issuing thread runs O += P(g - 1) V(g - 1) interleaved MMA by
+// MMA with S(g + 1) = Q K(g + 1)^T, two accumulators in flight (a chain of
+// MMAs into one accumulator waits on itself and runs at about half rate).
+// P.V takes its A operand from tensor memory, so shared memory only feeds Q,
+// K and V.  16 warps in four warpgroups:
+//   warps 0-3, 4-7  softmax: one thread per (row, column half): tcgen05.ld of
+//       64 scores, causal mask where a tile crosses the row's position, the
+//       row max combined with the other half's through shared memory, online
+//       softmax in base 2 with a reference max that moves only by more than
+//       2^8 (O rescaled in TMEM then), P written to TMEM with tcgen05.st;
+//   warps 8-11  epilogue, one thread per row: O / l to the output (or the
+//       unnormalised partial and its (m, l) to the split workspace); with
+//       E4M3 caches also the converter that widens each 8-bit K/V tile to
+//       16 bits in shared memory (and rounds bf16 q to f16);
+//   warps 12, 14, 15  TMA: each item's query tile (two buffers), then
+//       128-token K and V tiles block by block through the block table into a
+//       ring of slots, in the order the tensor core consumes them: a slot
+//       holds the two tiles one MMA phase reads, V(g) and K(g + 2), behind
+//       one barrier; a warp waits about 130 cycles on each box it issues, so
+//       the boxes are spread over three warps (warp 12 arms the byte count);
+//   warp 13     the MMA issuer: per phase it waits for one ring slot and one
+//       P buffer, issues 16 MMAs, and commits one barrier that tells the
+//       softmax both that S(g + 2) is ready and that P buffer g & 1 is free.
 // Every mbarrier wait gives up after about one second (error bit); a warp
 // that gives up raises a shared abort flag that stops the others, and
 // in-flight MMAs and TMA loads are drained (bounded) before the tensor
@@ -57,40 +62,62 @@ constexpr int kErrContextLen = 0x2;
 constexpr int kErrTimeout = 0x8;
 constexpr int kErrLayout = 0x10;
 
-constexpr int kHalfBytes = kTcRows * 128;      // 64 channels (128 bytes) of 128 rows
-constexpr int kPBytes = kTcRows * kTcTok * 2;  // one P tile, 16-bit
-constexpr int kProdWarp = 12, kMmaWarp = 13;
-// mbarriers (8 bytes each): q full / empty, S full / free, P full, P.V done,
-// O full / free and l ready per query tile; full / empty per ring slot; drain
-constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarSFull = 4, kBarSFree = 6, kBarPFull = 8, kBarPvDone = 10,
-              kBarOFull = 12, kBarOFree = 14, kBarLReady = 16, kBarSlotFull = 18,
-              kBarSlotEmpty = kBarSlotFull + kTcMaxSlots, kBarDrain = kBarSlotEmpty + kTcMaxSlots,
-              kNumBars = kBarDrain + 1;
-// after the barriers: abort flag, TMEM address, item -> sequence table, then
-// the row sums and reference maxima handed to the epilogue ([2][128] each)
+constexpr int kHalfBytes = kTcRows * 128;  // 64 channels (128 bytes) of 128 rows
+constexpr int kStageOff = kHalfBytes;      // E4M3 tile inside a ring slot (see slot_bytes)
+constexpr int kProdWarp = 12, kMmaWarp = 13;  // warps 14, 15 issue TMA boxes too
+constexpr int kProdWarps = 3;
+// tensor memory columns
+constexpr uint32_t kTmS = 0, kTmP = 256, kTmO = 384;
+// mbarriers (8 bytes each): q full / empty / converted per q buffer; phase
+// done, P full and max exchange per score buffer; O full / free and l ready;
+// full / empty / converted per ring slot; drain.  "Phase done" b completes
+// when the MMAs of a phase finish: those of phase e (P.V(e) and S(e + 2), or
+// S(e + 2) alone for e = -2, -1) complete barrier (e & 1) for the
+// ((e + 2) >> 1)-th time.
+constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarQConv = 4, kBarPh = 6, kBarPFull = 8, kBarXchg = 10,
+              kBarOFull = 12, kBarOFree = 13, kBarLReady = 14, kBarSlotFull = 15,
+              kBarSlotEmpty = kBarSlotFull + kTcMaxSlots, kBarSlotConv = kBarSlotEmpty + kTcMaxSlots,
+              kBarDrain = kBarSlotConv + kTcMaxSlots, kNumBars = kBarDrain + 1;
+// after the barriers: abort flag, TMEM address, this CTA's item -> sequence
+// and context-length tables, the row-max exchange [2][2][128], the row sums
+// [2][128] and reference maxima [128] handed to the epilogue, and the rows' q
+// scales [2][128]
 constexpr int kAbortOff = kNumBars * 8, kTmemOff = kAbortOff + 4, kSeqTabOff = kTmemOff + 4;
-constexpr int kLmOff = kSeqTabOff + kTcMaxRanked * 4;
-constexpr int kTailBytes = kLmOff + 2 * 2 * kTcRows * 4;
+constexpr int kLenTabOff = kSeqTabOff + kTcMaxRanked * 4;
+constexpr int kXchgOff = kLenTabOff + kTcMaxRanked * 4;
+constexpr int kLOff = kXchgOff + 2 * 2 * kTcRows * 4;
+constexpr int kMOff = kLOff + 2 * kTcRows * 4;
+constexpr int kQscOff = kMOff + kTcRows * 4;
+constexpr int kTailBytes = (kQscOff + 2 * kTcRows * 4 + 15) / 16 * 16;
 constexpr int kSmemLimit = 227 * 1024;
 // A row's reference max moves only when a tile exceeds it by more than this
 // (base 2): probabilities stay below 2^8 and O is rescaled rarely.
 constexpr float kRescaleThreshold = 8.f;
-// registers a thread of each warpgroup holds after setmaxnreg (x128 threads:
-// 2 x 184 + 72 + 72 = 512 = the 128 a thread of the 512 is launched with)
-constexpr int kRegsSoftmax = 184, kRegsEpilogue = 72, kRegsAux = 72;
 
 __host__ __device__ constexpr int tile_bytes(int D) { return kTcRows * D * 2; }
 
+// A ring slot holds two tiles (V(g), then K(g + 2)); each half holds one
+// 16-bit K or V tile in the MMA's operand layout.  With E4M3 caches the TMA
+// lands the 8-bit tile at kStageOff of its half and the converter widens it
+// there: for head_dim 128 in place (the 8-bit row r sits where the second
+// channel half of 16-bit row r goes, and only the thread that owns row r
+// touches either), for head_dim 64 in an extra 8 KB behind the 16-bit tile.
+__host__ __device__ constexpr int half_bytes(int D, int fp8) {
+  return (fp8 && D == 64) ? tile_bytes(D) + kTcRows * 64 : tile_bytes(D);
+}
+__host__ __device__ constexpr int slot_bytes(int D, int fp8) { return 2 * half_bytes(D, fp8); }
+
 struct Layout {
-  int q, p, ring, tail, total;
+  int q, ring, slot, tail, total;
 };
 
-__host__ __device__ inline Layout layout_of(int D, int NQ, int nslot) {
+// two q buffers (one per item parity), the ring, the tail
+__host__ __device__ inline Layout layout_of(int D, int nslot, int fp8) {
   Layout L;
   L.q = 0;
-  L.p = NQ * tile_bytes(D);
-  L.ring = L.p + NQ * kPBytes;
-  L.tail = L.ring + nslot * tile_bytes(D);
+  L.ring = 2 * tile_bytes(D);
+  L.slot = slot_bytes(D, fp8);
+  L.tail = L.ring + nslot * L.slot;
   L.total = L.tail + kTailBytes;
   return L;
 }
@@ -130,12 +157,45 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+// Four E4M3 codes (first element in the low byte) widened exactly to two
+// f16x2 words: codes 0, 1 to `lo`, codes 2, 3 to `hi` (the conversion
+// instruction reads each 16-bit half of the word).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 c0, c1;\n\t"
+      "mov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(four));
+}
 // L2 prefetch of a 3-D tensor box (the next item's query tile).
 __device__ __forceinline__ void tma_prefetch_3d(const void* map, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(c0), "r"(c1), "r"(c2)
                : "memory");
+}
+// The MMAs with no memory clobber: the issuing thread's ordering with the
+// other warps goes through mbarriers and tcgen05 fences, not through C++
+// memory, so the compiler may keep its operands in registers around them.
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
 // Length key of the longest-first order: 128 buckets, 4 per power of two,
@@ -148,42 +208,37 @@ __device__ __forceinline__ int length_bucket(int L) {
 }
 
 struct Item {
-  int s, h, qp, run, L;
-  int j0[2], ntok[2];  // first new token and token count of each query tile (0: no tile)
+  int s, h, qt, run, L;
+  int j0, ntok;        // first new token of the query tile and how many it holds
   int kv_lo, kv_hi;    // KV tokens the item reads
   int ntiles;          // 128-token KV tiles
   bool valid;          // false: a run past the end of its context (nothing to write)
   bool final_out;      // the item writes normalised outputs (not a split partial)
 };
 
-// Work item k of this CTA (global index blockIdx.x + k * gridDim.x).
-__device__ Item item_of(const TcParams& p, const int* seq_tab, int k) {
+// Work item k of this CTA (global index blockIdx.x + k * gridDim.x).  With
+// at most kTcMaxRanked items per CTA their sequences and context lengths
+// come from the tables built at start-up (shared memory, no global load on
+// the pipeline's path).
+__device__ Item item_of(const TcParams& p, const int* seq_tab, const int* len_tab, bool tabs, int k) {
   Item it;
   const int idx = blockIdx.x + k * gridDim.x;
-  const int per_h = p.n_qp * p.R;
+  const int per_h = p.n_qt * p.R;
   const int per_seq = p.Hkv * per_h;
   const int rank = idx / per_seq;
   int rem = idx - rank * per_seq;
   it.h = rem / per_h;
   rem -= it.h * per_h;
-  const int qp = p.n_qp - 1 - rem / p.R;
-  it.qp = qp;
+  it.qt = p.n_qt - 1 - rem / p.R;
   it.run = rem % p.R;
-  it.s = p.rank_seqs ? seq_tab[k] : rank;
+  it.s = tabs ? seq_tab[k] : rank;
   int lmax = p.maxB * p.bs;
   if (p.partition_size > 0) lmax = min(lmax, p.Pmax * p.partition_size);
-  const int L = min(max(__ldg(p.context_lens + it.s), 0), lmax);
+  const int L = min(max(tabs ? len_tab[k] : __ldg(p.context_lens + it.s), 0), lmax);
   it.L = L;
-  int jl = -1;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int j0 = (qp * p.NQ + i) * p.T;
-    const int n = i < p.NQ ? min(max(p.C - j0, 0), p.T) : 0;
-    it.j0[i] = j0;
-    it.ntok[i] = n;
-    if (n > 0) jl = j0 + n - 1;
-  }
-  int lo = 0, hi = min(L, L - p.C + jl + 1);  // the last live row attends to tokens < hi
+  it.j0 = it.qt * p.T;
+  it.ntok = min(p.C - it.j0, p.T);
+  int lo = 0, hi = min(L, L - p.C + it.j0 + it.ntok);  // the last row attends to tokens < hi
   it.valid = true;
   it.final_out = true;
   if (p.partition_size > 0) {
@@ -200,9 +255,19 @@ __device__ Item item_of(const TcParams& p, const int* seq_tab, int k) {
   return it;
 }
 
+// Position in the stream of K/V tiles of this CTA's items that have any:
+// item k (its ordinal among such items) and tile t.
+struct Cursor {
+  int k, ord, t;
+  Item it;
+};
+
+template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  constexpr int TB = tile_bytes(D);
+  constexpr int HALVES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = smem_u32(smem);
@@ -212,45 +277,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) atomicOr(p.err, kErrLayout);
     return;
   }
-  const Layout Ly = layout_of(p.D, p.NQ, p.nslot);
-  const int TB = tile_bytes(p.D);
+  const Layout Ly = layout_of(D, p.nslot, p.fp8);
   const uint32_t bar0 = base + Ly.tail;
   auto bar = [&](int k) -> uint32_t { return bar0 + 8u * k; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.tail + kAbortOff);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly.tail + kTmemOff);
-  int* seq_tab = reinterpret_cast<int*>(smem + Ly.tail + kSeqTabOff);
-  float* l_buf = reinterpret_cast<float*>(smem + Ly.tail + kLmOff);  // [2][128]
-  float* m_buf = l_buf + 2 * kTcRows;                                 // [2][128]
-  auto q_smem = [&](int i) -> uint32_t { return base + Ly.q + i * TB; };
-  auto p_smem = [&](int i) -> uint32_t { return base + Ly.p + i * kPBytes; };
-  auto slot_smem = [&](int k) -> uint32_t { return base + Ly.ring + k * TB; };
+  uint8_t* tail = smem + Ly.tail;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + kAbortOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + kTmemOff);
+  int* seq_tab = reinterpret_cast<int*>(tail + kSeqTabOff);
+  int* len_tab = reinterpret_cast<int*>(tail + kLenTabOff);
+  float* xchg = reinterpret_cast<float*>(tail + kXchgOff);  // [2 buffers][2 halves][128]
+  float* l_buf = reinterpret_cast<float*>(tail + kLOff);    // [2 halves][128]
+  float* m_buf = reinterpret_cast<float*>(tail + kMOff);    // [128]
+  float* qsc = reinterpret_cast<float*>(tail + kQscOff);    // [2 q buffers][128]
+  const uint32_t q_base = base + Ly.q, ring_base = base + Ly.ring;
+  const int slot_b = Ly.slot, half_b = half_bytes(D, p.fp8);
   const int nk = (p.total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                  static_cast<int>(gridDim.x);  // this CTA's work items
+  const bool tabs = nk <= kTcMaxRanked;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarQFull + i), 1);
       mbar_init(bar(kBarQEmpty + i), 1);
-      mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSFree + i), kTcRows);
-      mbar_init(bar(kBarPFull + i), kTcRows);
-      mbar_init(bar(kBarPvDone + i), 1);
-      mbar_init(bar(kBarOFull + i), 1);
-      mbar_init(bar(kBarOFree + i), kTcRows);
-      mbar_init(bar(kBarLReady + i), kTcRows);
+      mbar_init(bar(kBarQConv + i), kTcRows);
+      mbar_init(bar(kBarPh + i), 1);
+      mbar_init(bar(kBarPFull + i), 2 * kTcRows);
+      mbar_init(bar(kBarXchg + i), 2 * kTcRows);
     }
+    mbar_init(bar(kBarOFull), 1);
+    mbar_init(bar(kBarOFree), kTcRows);
+    mbar_init(bar(kBarLReady), 2 * kTcRows);
     for (int k = 0; k < p.nslot; ++k) {
       mbar_init(bar(kBarSlotFull + k), 1);
       mbar_init(bar(kBarSlotEmpty + k), 1);
+      mbar_init(bar(kBarSlotConv + k), kTcRows);
     }
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   // Longest-first order: the sequence of each of this CTA's items, from a
-  // histogram of context-length buckets built in the (not yet used) P area.
-  if (p.rank_seqs) {
-    int* hist = reinterpret_cast<int*>(smem + Ly.p);  // [128] counts, then [128] offsets
+  // histogram of context-length buckets built in the (not yet used) ring;
+  // then the items' context lengths.
+  if (tabs && p.rank_seqs) {
+    int* hist = reinterpret_cast<int*>(smem + Ly.ring);  // [128] counts, then [128] offsets
     int* offs = hist + 128;
     if (tid < 128) hist[tid] = 0;
     __syncthreads();
@@ -277,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncthreads();
-    const int per_seq = p.Hkv * p.n_qp * p.R;
+    const int per_seq = p.Hkv * p.n_qt * p.R;
     for (int k = warp; k < nk; k += kTcThreads / 32) {
       const int rank = (static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x)) / per_seq;
       // the bucket holding rank, then the rank's place among that bucket's
@@ -308,6 +378,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (lane == 0) seq_tab[k] = found;
     }
+  } else if (tabs) {
+    const int per_seq = p.Hkv * p.n_qt * p.R;
+    for (int k = tid; k < nk; k += kTcThreads) seq_tab[k] = (static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x)) / per_seq;
+  }
+  if (tabs) {
+    __syncthreads();
+    for (int k = tid; k < nk; k += kTcThreads) len_tab[k] = __ldg(p.context_lens + seq_tab[k]);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -317,8 +394,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto tS = [&](int i) -> uint32_t { return tmem + 128u * i; };
-  auto tO = [&](int i) -> uint32_t { return tmem + 256u + 128u * i; };
   auto fail = [&]() {
     if (lane == 0) {
       atomicOr(p.err, kErrTimeout);
@@ -328,207 +403,287 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // the next item with K/V tiles to process, at or after item k
   auto next_active = [&](int k, Item& it) -> int {
     for (; k < nk; ++k) {
-      it = item_of(p, seq_tab, k);
+      it = item_of(p, seq_tab, len_tab, tabs, k);
       if (it.valid && it.ntiles > 0) return k;
     }
     return nk;
   };
+  auto cur_start = [&](Cursor& c) {
+    c.k = next_active(0, c.it);
+    c.ord = 0;
+    c.t = 0;
+  };
+  auto cur_next = [&](Cursor& c) {
+    if (++c.t < c.it.ntiles) return;
+    c.k = next_active(c.k + 1, c.it);
+    ++c.ord;
+    c.t = 0;
+  };
+  // tokens of KV tile t of an item that lie in its range
+  auto valid_tokens = [](const Item& it, int t) { return min(kTcTok, it.kv_hi - (it.kv_lo + t * kTcTok)); };
 
   if (warp >= 12) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsAux) : "memory");
-    if (warp == kProdWarp) {
-      // ============================ TMA producer ============================
-      if (lane == 0) {
+    if (warp != kMmaWarp) {
+      // ============================ TMA producers ============================
+      // producer w issues the boxes i = w, w + 3, ... of each tile: box i is
+      // 64-channel half i % HALVES of block i / HALVES (one box per block
+      // for E4M3); this lane's box is i = 3 lane + w
+      const int w = warp == kProdWarp ? 0 : warp - 13;
+      const bool lead = w == 0;  // arms the byte counts and loads the query tiles
+      const int bpb = p.fp8 ? 1 : HALVES;  // boxes per block
+      const int my_box = kProdWarps * lane + w;
+      const int my_blk = my_box / bpb, my_half = my_box % bpb;
+      int rslot = 0, rphase = 0, n = 0;  // ring step n: its slot and phase parity
+      if (lead && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
       }
-      const int halves = p.D / 64;
-      int n = 0, ql[2] = {0, 0};
       bool ok = true;
-      // K or V tile t of item `it` into the next ring slot
-      auto load_kv = [&](const Item& it, int t, bool is_v) -> bool {
-        const int slot = n % p.nslot;
-        if (n >= p.nslot && !mbar_wait(bar(kBarSlotEmpty + slot), ((n / p.nslot) - 1) & 1)) return false;
-        const int tok0 = it.kv_lo + t * kTcTok;
-        const int tok1 = min(tok0 + kTcTok, it.kv_hi);
-        const int b0 = tok0 / p.bs;
-        const int nb = (tok1 - 1) / p.bs - b0 + 1;
-        const uint32_t full = bar(kBarSlotFull + slot);
-        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * p.bs * p.D * 2));
-        __syncwarp();
-        const int* bt_row = p.block_tables + static_cast<int64_t>(it.s) * p.maxB;
-        for (int b = lane; b < nb; b += 32) {
-          const int phys = __ldg(bt_row + b0 + b);
-          if (!is_v && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
-          const uint32_t dst = slot_smem(slot) + b * p.bs * 128;
-          for (int hf = 0; hf < halves; ++hf)
-            tma_load_4d(dst + hf * kHalfBytes, is_v ? &tmV : &tmK, full, 64 * hf, 0, it.h, phys);
+      // blocks of a tile: at most 128 / 8 = 16
+      auto tile_blocks = [&](const Cursor& c, int& b0) -> int {
+        const int tok0 = c.it.kv_lo + c.t * kTcTok;
+        b0 = tok0 / p.bs;
+        return (tok0 + valid_tokens(c.it, c.t) - 1) / p.bs - b0 + 1;
+      };
+      // the block id of this lane's box in the cursor's tile, read ahead of
+      // the load that needs it (the block-table read is a dependent global load)
+      auto tile_id = [&](const Cursor& c) -> int {
+        if (c.k >= nk) return -1;
+        int b0;
+        const int nb = tile_blocks(c, b0);
+        return my_blk < nb ? __ldg(p.block_tables + static_cast<int64_t>(c.it.s) * p.maxB + b0 + my_blk) : -1;
+      };
+      auto tile_bytes_of = [&](const Cursor& c) -> uint32_t {
+        int b0;
+        return static_cast<uint32_t>(tile_blocks(c, b0) * p.bs * D * (p.fp8 ? 1 : 2));
+      };
+      // this lane's box of a K or V tile into half `hf2` of the step's slot
+      auto issue_tile = [&](const Cursor& c, bool is_v, int phys, uint32_t dst, uint32_t full) {
+        int b0;
+        const int nb = tile_blocks(c, b0);
+        if (my_blk < nb) {
+          if (!is_v && my_half == 0 && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks))
+            atomicOr(p.err, kErrBlockId);
+          if (p.fp8)  // one box of D bytes per row: the 8-bit tile, widened later
+            tma_load_4d(dst + kStageOff + my_blk * p.bs * D, is_v ? &tmV : &tmK, full, 0, 0, c.it.h, phys);
+          else
+            tma_load_4d(dst + my_blk * p.bs * 128 + my_half * kHalfBytes, is_v ? &tmV : &tmK, full, 64 * my_half, 0,
+                        c.it.h, phys);
         }
+      };
+      // an item's query tile (G heads x T tokens per 64-channel half) into q
+      // buffer ord & 1, once the item two before it has finished with it
+      int nq = 0;  // query tiles loaded
+      auto load_q = [&](const Cursor& c) -> bool {
+        ++nq;
+        if (!lead) return true;
+        const int qb = c.ord & 1;
+        if (c.ord >= 2 && !mbar_wait(bar(kBarQEmpty + qb), ((c.ord - 2) >> 1) & 1)) return false;
+        if (lane == 0) {
+          const uint32_t full = bar(kBarQFull + qb);
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.G * p.T * 128 * HALVES));
+#pragma unroll
+          for (int hf = 0; hf < HALVES; ++hf)
+            tma_load_3d(q_base + qb * TB + hf * kHalfBytes, &tmQ, full, 64 * hf, c.it.h * p.G,
+                        c.it.s * p.C + c.it.j0);
+        }
+        __syncwarp();
+        return true;
+      };
+      // ring steps in the tensor core's order: step 0 = K(0), K(1); step
+      // e >= 1 = V(e - 1), K(e + 1).  V(g) reuses the block ids read for K(g):
+      // ids of the K tiles whose V is still to come wait in f0 (oldest), f1;
+      // the next K tile's ids are read as soon as the previous K is issued.
+      Cursor kc, vc;
+      cur_start(kc);
+      vc = kc;
+      int pre = tile_id(kc), f0 = -1, f1 = -1, nf = 0;
+      // one step: tile a (a V, or K(0) at step 0) into the first half, K of the
+      // K cursor (if any) into the second
+      auto step = [&](bool first) -> bool {
+        const int slot = rslot;
+        if (n >= p.nslot && !mbar_wait(bar(kBarSlotEmpty + slot), rphase ^ 1)) return false;
+        const uint32_t dst = ring_base + slot * slot_b, full = bar(kBarSlotFull + slot);
+        // tile a
+        Cursor ca = first ? kc : vc;
+        int ida;
+        if (first) {
+          if (kc.t == 0 && !load_q(kc)) return false;
+          ida = pre;
+          f0 = ida;
+          nf = 1;
+          cur_next(kc);
+          pre = tile_id(kc);
+        } else {
+          ida = f0;
+          f0 = f1;
+          --nf;
+          cur_next(vc);
+        }
+        // tile b: the next K, if there is one
+        const bool has_b = kc.k < nk;
+        Cursor cb = kc;
+        int idb = -1;
+        if (has_b) {
+          if (kc.t == 0 && !load_q(kc)) return false;
+          idb = pre;
+          if (nf == 0) f0 = idb; else f1 = idb;
+          ++nf;
+          cur_next(kc);
+          pre = tile_id(kc);
+        }
+        // the byte count may be armed after another producer's boxes have
+        // landed: the transaction count goes negative until then, and the
+        // phase cannot complete before the arrival that arms it
+        if (lead && lane == 0)
+          mbar_arrive_expect_tx(full, tile_bytes_of(ca) + (has_b ? tile_bytes_of(cb) : 0u));
+        __syncwarp();
+        issue_tile(ca, !first, ida, dst, full);
+        if (has_b) issue_tile(cb, false, idb, dst + half_b, full);
         __syncwarp();
         ++n;
-        return true;
-      };
-      // the item's query tiles (one TMA box per 64-channel half: G heads x T tokens)
-      auto load_q = [&](const Item& it) -> bool {
-        for (int i = 0; i < 2; ++i) {
-          if (it.ntok[i] == 0) continue;
-          if (ql[i] >= 1 && !mbar_wait(bar(kBarQEmpty + i), (ql[i] - 1) & 1)) return false;
-          if (lane == 0) {
-            const uint32_t full = bar(kBarQFull + i);
-            mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.G * p.T * 128 * halves));
-            for (int hf = 0; hf < halves; ++hf)
-              tma_load_3d(q_smem(i) + hf * kHalfBytes, &tmQ, full, 64 * hf, it.h * p.G, it.s * p.C + it.j0[i]);
-          }
-          __syncwarp();
-          ++ql[i];
+        if (++rslot == p.nslot) {
+          rslot = 0;
+          rphase ^= 1;
         }
         return true;
       };
-      Item cur;
-      int k = next_active(0, cur);
-      if (k < nk) ok = load_q(cur) && load_kv(cur, 0, false);
-      while (ok && k < nk) {
-        Item nxt;
-        const int kn = next_active(k + 1, nxt);
-        if (kn < nk && lane == 0) {  // the next item's query tiles into L2 ahead of time
-          for (int i = 0; i < 2; ++i)
-            if (nxt.ntok[i] > 0)
-              for (int hf = 0; hf < halves; ++hf)
-                tma_prefetch_3d(&tmQ, 64 * hf, nxt.h * p.G, nxt.s * p.C + nxt.j0[i]);
+      if (kc.k < nk) ok = step(true);
+      while (ok && vc.k < nk) {
+        if (*abort_flag) {
+          ok = false;
+          break;
         }
-        for (int t = 0; ok && t < cur.ntiles; ++t) {
-          if (*abort_flag) {
-            ok = false;
-            break;
-          }
-          // consumption order of the tensor core: K of the next tile (this
-          // item's, or the next item's first after its query tiles), then V
-          if (t + 1 < cur.ntiles)
-            ok = load_kv(cur, t + 1, false);
-          else if (kn < nk)
-            ok = load_q(nxt) && load_kv(nxt, 0, false);
-          if (ok) ok = load_kv(cur, t, true);
+        if (vc.t == 0 && lead && lane == 0) {  // the query tile of the item after next into L2 ahead of time
+          Item nx;
+          if (next_active(vc.k + 1, nx) < nk)
+            for (int hf = 0; hf < HALVES; ++hf) tma_prefetch_3d(&tmQ, 64 * hf, nx.h * p.G, nx.s * p.C + nx.j0);
         }
-        k = kn;
-        cur = nxt;
+        ok = step(false);
       }
       if (!ok) fail();
-      // every load issued lands before the CTA can exit
+      // every load issued lands before the CTA can exit (the lead producer
+      // armed every slot whose boxes any producer issued, so the last nslot
+      // phases complete once all those boxes land)
       for (int u = max(0, n - p.nslot); u < n; ++u) mbar_wait(bar(kBarSlotFull + u % p.nslot), (u / p.nslot) & 1);
-      for (int i = 0; i < 2; ++i)
-        if (ql[i] > 0) mbar_wait(bar(kBarQFull + i), (ql[i] - 1) & 1);
+      if (lead)
+        for (int u = max(0, nq - 2); u < nq; ++u) mbar_wait(bar(kBarQFull + (u & 1)), (u >> 1) & 1);
     } else if (warp == kMmaWarp) {
       // ============================= MMA issuer =============================
+      constexpr int KS = D / 16;  // k-steps of Q.K^T
       const uint32_t id_qk = tc_idesc_f16(p.bf16 != 0, false, kTcRows, kTcTok);
-      const uint32_t id_pv = tc_idesc_f16(p.bf16 != 0, true, kTcRows, p.D);
-      const int KS = p.D / 16;
-      int n = 0, qc[2] = {0, 0}, sc[2] = {0, 0}, pc[2] = {0, 0}, oc[2] = {0, 0};
-      bool ok = true, issued = false;
-      auto wait_q = [&](const Item& it) -> bool {
-        for (int i = 0; i < 2; ++i) {
-          if (it.ntok[i] == 0) continue;
-          if (!mbar_wait(bar(kBarQFull + i), qc[i] & 1)) return false;
-          ++qc[i];
+      const uint32_t id_pv = tc_idesc_f16(p.bf16 != 0, true, kTcRows, D);
+      const int ready_bar = p.fp8 ? kBarSlotConv : kBarSlotFull;  // the slot holds 16-bit tiles
+      const int q_bar = p.q_scale_rows ? kBarQConv : kBarQFull;
+      int rslot = 0, rphase = 0;  // ring step: slot and phase parity
+      auto ring_next = [&]() {
+        if (++rslot == p.nslot) {
+          rslot = 0;
+          rphase ^= 1;
         }
-        return true;
       };
-      // S_i = Q_i K^T for the item's query tiles, MMA by MMA alternating tiles
-      auto s_phase = [&](const Item& it, int t) -> bool {
-        const int slot = n % p.nslot;
-        if (!mbar_wait(bar(kBarSlotFull + slot), (n / p.nslot) & 1)) return false;
-        for (int i = 0; i < 2; ++i)
-          if (it.ntok[i] > 0 && sc[i] >= 1 && !mbar_wait(bar(kBarSFree + i), (sc[i] - 1) & 1)) return false;
+      bool ok = true, issued = false;
+      Cursor sc, pc;  // the tiles whose scores (sc) and P.V (pc) come next
+      cur_start(sc);
+      pc = sc;
+      int sg = 0;  // score tiles issued
+      // S(sg) = Q K^T from `kaddr` into score buffer sg & 1 (after its item's q tile)
+      auto s_issue = [&](uint32_t kaddr) -> bool {
+        if (sc.t == 0 && !mbar_wait(bar(q_bar + (sc.ord & 1)), (sc.ord >> 1) & 1)) return false;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t kb = slot_smem(slot);
+          const uint64_t qd = tc_desc_sw128(q_base + (sc.ord & 1) * TB, 16, 1024);
+          const uint64_t kd = tc_desc_sw128(kaddr, 16, 1024);
+          const uint32_t d = tmem + kTmS + 128u * (sg & 1);
+#pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            const uint64_t bdesc = tc_desc_sw128(kb + off, 16, 1024);
-            for (int i = 0; i < 2; ++i)
-              if (it.ntok[i] > 0) tc_mma_f16(tS(i), tc_desc_sw128(q_smem(i) + off, 16, 1024), bdesc, id_qk, kk > 0);
+            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_ss(d, qd + off, kd + off, id_qk, kk > 0);
           }
-          for (int i = 0; i < 2; ++i)
-            if (it.ntok[i] > 0) tc_commit(bar(kBarSFull + i));
-          tc_commit(bar(kBarSlotEmpty + slot));
-          if (t == it.ntiles - 1)
-            for (int i = 0; i < 2; ++i)
-              if (it.ntok[i] > 0) tc_commit(bar(kBarQEmpty + i));
+          tc_commit(bar(kBarPh + (sg & 1)));  // phase sg - 2: S(sg) alone
+          if (sc.t == sc.it.ntiles - 1) tc_commit(bar(kBarQEmpty + (sc.ord & 1)));
         }
         __syncwarp();
-        for (int i = 0; i < 2; ++i) sc[i] += it.ntok[i] > 0;
-        ++n;
+        ++sg;
+        cur_next(sc);
         issued = true;
         return true;
       };
-      // O_i += P_i V over the tile's valid tokens
-      auto pv_phase = [&](const Item& it, int t) -> bool {
-        const int slot = n % p.nslot;
-        if (!mbar_wait(bar(kBarSlotFull + slot), (n / p.nslot) & 1)) return false;
-        const int valid = min(kTcTok, it.kv_hi - (it.kv_lo + t * kTcTok));
+      // step 0: S(0) and S(1) alone
+      if (sc.k < nk) {
+        ok = mbar_wait(bar(ready_bar + rslot), rphase) && s_issue(ring_base + rslot * slot_b);
+        if (ok && sc.k < nk) ok = s_issue(ring_base + rslot * slot_b + half_b);
+        if (ok && lane == 0) tc_commit(bar(kBarSlotEmpty + rslot));
+        __syncwarp();
+        ring_next();
+      }
+      int g = 0;  // P.V tiles issued
+      while (ok && pc.k < nk) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        // phase g: P.V(g) with S(g + 2), both tiles in the ring step's slot;
+        // the probabilities, and at an item's first tile the O buffer (read by
+        // the previous item's epilogue).  S(g + 2) reuses the score buffer of
+        // S(g), which its softmax has read before arriving on P(g).
+        const int slot = rslot;
+        if (!(ok = mbar_wait(bar(ready_bar + slot), rphase))) break;
+        const int valid = valid_tokens(pc.it, pc.t);
         const int nks = (valid + 15) / 16;
-        const uint32_t vb = slot_smem(slot);
-        if (valid < nks * 16) {
+        const uint32_t vb = ring_base + slot * slot_b, kb = vb + half_b;
+        if (valid < nks * 16 && !p.fp8) {
           // rows past the context in the last k-step hold pool bytes past the
           // context or stale tiles: zero them so that 0 * junk cannot make NaN
-          const int rows = nks * 16 - valid, halves = p.D / 64;
-          for (int w = lane; w < rows * 8 * halves; w += 32) {
-            const int row = valid + w / (8 * halves), rest = w % (8 * halves);
+          // (the E4M3 converter zeroes them itself)
+          const int rows = nks * 16 - valid;
+          for (int w = lane; w < rows * 8 * HALVES; w += 32) {
+            const int row = valid + w / (8 * HALVES), rest = w % (8 * HALVES);
             st_shared_v4(vb + (rest / 8) * kHalfBytes + row * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           __syncwarp();
         }
-        for (int i = 0; i < 2; ++i) {
-          if (it.ntok[i] == 0) continue;
-          if (!mbar_wait(bar(kBarPFull + i), pc[i] & 1)) return false;
-          // O_i was last read by the epilogue of the previous item using tile i
-          if (t == 0 && oc[i] >= 1 && !mbar_wait(bar(kBarOFree + i), (oc[i] - 1) & 1)) return false;
-        }
+        if (!(ok = mbar_wait(bar(kBarPFull + (g & 1)), (g >> 1) & 1))) break;
+        if (pc.t == 0 && pc.ord >= 1 && !(ok = mbar_wait(bar(kBarOFree), (pc.ord - 1) & 1))) break;
+        const bool with_s = sc.k < nk;
+        if (with_s && sc.t == 0 && !(ok = mbar_wait(bar(q_bar + (sc.ord & 1)), (sc.ord >> 1) & 1))) break;
         tc_fence_after();
         if (lane == 0) {
-          for (int kk = 0; kk < nks; ++kk) {
-            const uint64_t bdesc = tc_desc_sw128(vb + kk * 2048, kHalfBytes, 1024);
-            const uint32_t aoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            for (int i = 0; i < 2; ++i)
-              if (it.ntok[i] > 0)
-                tc_mma_f16(tO(i), tc_desc_sw128(p_smem(i) + aoff, 16, 1024), bdesc, id_pv, (t > 0 || kk > 0));
+          const uint32_t dO = tmem + kTmO, aP = tmem + kTmP + 64u * (g & 1);
+          const uint64_t vd = tc_desc_sw128(vb, kHalfBytes, 1024);
+          const uint32_t acc0 = pc.t > 0 ? 1u : 0u;
+          if (with_s) {
+            const uint64_t qd = tc_desc_sw128(q_base + (sc.ord & 1) * TB, 16, 1024);
+            const uint64_t kd = tc_desc_sw128(kb, 16, 1024);
+            const uint32_t dS = tmem + kTmS + 128u * (sg & 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              if (kk < nks) mma_ts(dO, aP + 8 * kk, vd + ((kk * 2048) >> 4), id_pv, kk > 0 ? 1u : acc0);
+              if (kk < KS) {
+                const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                mma_ss(dS, qd + off, kd + off, id_qk, kk > 0);
+              }
+            }
+            if (sc.t == sc.it.ntiles - 1) tc_commit(bar(kBarQEmpty + (sc.ord & 1)));
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if (kk < nks) mma_ts(dO, aP + 8 * kk, vd + ((kk * 2048) >> 4), id_pv, kk > 0 ? 1u : acc0);
           }
-          for (int i = 0; i < 2; ++i)
-            if (it.ntok[i] > 0) tc_commit(bar(kBarPvDone + i));
+          tc_commit(bar(kBarPh + (g & 1)));  // phase g: S(g + 2) ready, P buffer g & 1 free
           tc_commit(bar(kBarSlotEmpty + slot));
-          if (t == it.ntiles - 1)
-            for (int i = 0; i < 2; ++i)
-              if (it.ntok[i] > 0) tc_commit(bar(kBarOFull + i));
+          if (pc.t == pc.it.ntiles - 1) tc_commit(bar(kBarOFull));
         }
         __syncwarp();
-        for (int i = 0; i < 2; ++i) {
-          pc[i] += it.ntok[i] > 0;
-          if (t == it.ntiles - 1) oc[i] += it.ntok[i] > 0;
+        ++g;
+        cur_next(pc);
+        if (with_s) {
+          ++sg;
+          cur_next(sc);
         }
-        ++n;
-        return true;
-      };
-      Item cur;
-      int k = next_active(0, cur);
-      if (k < nk) ok = wait_q(cur) && s_phase(cur, 0);
-      while (ok && k < nk) {
-        Item nxt;
-        const int kn = next_active(k + 1, nxt);
-        for (int t = 0; t < cur.ntiles; ++t) {
-          if (*abort_flag) {
-            ok = false;
-            break;
-          }
-          // the next tile's scores overlap this tile's softmax
-          if (t + 1 < cur.ntiles)
-            ok = s_phase(cur, t + 1);
-          else if (kn < nk)
-            ok = wait_q(nxt) && s_phase(nxt, 0);
-          if (!ok || !(ok = pv_phase(cur, t))) break;
-        }
-        k = kn;
-        cur = nxt;
+        ring_next();
       }
       if (!ok) fail();
       // every MMA issued has completed before tensor memory is released
@@ -537,51 +692,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         mbar_wait(bar(kBarDrain), 0);
       }
-    }  // warps 14, 15: idle
+    }
   } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax) : "memory");
-    // ===================== softmax: one thread per row =====================
-    const int i = warp >> 2;  // query tile
-    const int r = tid & 127;  // row = TMEM lane
+    // ============ softmax: one thread per (row, half of the columns) ============
+    const int hh = warp >> 2;  // column half of every tile: tokens 64 hh .. 64 hh + 63
+    const int r = tid & 127;   // row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t prow = p_smem(i) + r * 128;
-    const int rsw = r & 7;
-    int sc = 0, pcnt = 0, oc = 0;
+    const uint32_t tS = tmem + kTmS + lane_off + 64u * hh;
+    const uint32_t tP = tmem + kTmP + lane_off + 32u * hh;
+    const uint32_t tO = tmem + kTmO + lane_off + (D / 2) * hh;
+    int g = 0, ord = 0;
     bool ok = true;
     for (int k = 0; ok && k < nk; ++k) {
-      const Item it = item_of(p, seq_tab, k);
-      if (!it.valid || it.ntiles == 0 || it.ntok[i] == 0) continue;
-      const bool live = r < it.ntok[i] * p.G;
-      const int pos = live ? it.L - p.C + it.j0[i] + r / p.G : -1;
+      const Item it = item_of(p, seq_tab, len_tab, tabs, k);
+      if (!it.valid || it.ntiles == 0) continue;
+      const bool live = r < it.ntok * p.G;
+      const int pos = live ? it.L - p.C + it.j0 + r / p.G : -1;
       const int last = min(pos, it.kv_hi - 1);  // last token this row attends to
-      float m = -CUDART_INF_F, l = 0.f;         // reference max (base 2) and row sum
-      for (int t = 0; t < it.ntiles; ++t) {
+      float sl2 = p.scale_log2;                 // this row's score multiplier (base 2)
+      const int qb = ord & 1;
+      if (p.q_scale_rows) {
+        // the converter rounded this row of q to f16 after scaling it by 2^e:
+        // 2^-e goes into the row's score multiplier
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQConv + qb), (ord >> 1) & 1)))) break;
+        sl2 *= qsc[qb * kTcRows + r];
+      }
+      float m = -CUDART_INF_F, l = 0.f;  // reference max (base 2) and this half's row sum
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarSFull + i), sc & 1)))) break;
+        const int b = g & 1, ph = (g >> 1) & 1;
+        // S(g) is ready, and P buffer b free, once phase g - 2 is done
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPh + b), ph)))) break;
         tc_fence_after();
-        float sv[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tS(i) + lane_off + c * 32, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
+        float sv[64];
+        tmem_ld32(tS + 128u * b, *reinterpret_cast<float(*)[32]>(sv));
+        tmem_ld32(tS + 128u * b + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(kBarSFree + i));  // the next scores may overwrite the buffer
-        ++sc;
-        const int lim = last - (it.kv_lo + t * kTcTok);  // last visible column of this tile
-        if (!__all_sync(0xFFFFFFFFu, lim >= kTcTok - 1)) {
+        const int lim = last - (it.kv_lo + t * kTcTok + 64 * hh);  // last visible column of this half
+        if (!__all_sync(0xFFFFFFFFu, lim >= 63)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) sv[c] = (c <= lim) ? sv[c] : -CUDART_INF_F;
+          for (int c = 0; c < 64; ++c) sv[c] = (c <= lim) ? sv[c] : -CUDART_INF_F;
         }
         float mx8[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx8[a] = -CUDART_INF_F;
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], sv[c], sv[c + 1]);
-        const float mx = p.scale_log2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int c = 0; c < 64; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], sv[c], sv[c + 1]);
+        // the row max over both halves: exchange through shared memory
+        float* xs = xchg + b * 2 * kTcRows;
+        xs[hh * kTcRows + r] = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        mbar_arrive(bar(kBarXchg + b));
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarXchg + b), ph)))) break;
+        const float mx = sl2 * fmaxf(xs[r], xs[kTcRows + r]);
         const bool bump = mx > m + kRescaleThreshold;  // false while both are -inf
         float alpha = 1.f;
         if (bump) {
@@ -589,10 +755,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m = mx;
         }
         const float m_use = m == -CUDART_INF_F ? 0.f : m;
-        const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_use, -m_use);
+        const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-m_use, -m_use);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
+        for (int c = 0; c < 64; c += 2) {
           float lo, hi;
           f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), sc2, nm2), lo, hi);
           sv[c] = ex2(lo);
@@ -603,118 +769,253 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int a = 0; a < 4; ++a) f2unpack(acc[a], sum8[2 * a], sum8[2 * a + 1]);
         l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
-        uint32_t pw[64];
+        uint32_t pw[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pw[c] = pack16(sv[2 * c], sv[2 * c + 1], p.bf16);
-        // P_i and O_i are free once the previous P.V of this tile slot has completed
-        if (pcnt >= 1 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPvDone + i), (pcnt - 1) & 1)))) break;
+        for (int c = 0; c < 32; ++c) pw[c] = pack16(sv[2 * c], sv[2 * c + 1], p.bf16);
         if (t > 0 && __any_sync(0xFFFFFFFFu, bump)) {
-          // rows whose reference moved rescale their O row (others multiply by 1)
+          // rows whose reference moved rescale their half of the O row once
+          // P.V(g - 1) has landed (the others multiply by 1)
+          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPh + (b ^ 1)), ((g + 1) >> 1) & 1)))) break;
           tc_fence_after();
-          for (int c = 0; c < p.D / 32; ++c) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
             float o[32];
-            tmem_ld32(tO(i) + lane_off + c * 32, o);
+            tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tO(i) + lane_off + c * 32, o);
+            tmem_st32(tO + 32 * c, o);
           }
-          tmem_wait_st();
         }
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(prow + (c >> 3) * kHalfBytes + (((c & 7) ^ rsw) << 4), pw[4 * c], pw[4 * c + 1],
-                       pw[4 * c + 2], pw[4 * c + 3]);
-        fence_proxy_async_smem();
+        tmem_st32(tP + 64u * b, pw);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(kBarPFull + i));
-        ++pcnt;
+        mbar_arrive(bar(kBarPFull + b));
       }
       if (!ok) break;
-      // hand (l, m) to the epilogue; the slot was read by the previous item's epilogue
-      if (oc >= 1 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFree + i), (oc - 1) & 1)))) break;
-      l_buf[i * kTcRows + r] = l;
-      m_buf[i * kTcRows + r] = m;
-      mbar_arrive(bar(kBarLReady + i));
-      ++oc;
+      // hand (l, m) to the epilogue; the slots were read by the previous item's
+      if (ord >= 1 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFree), (ord - 1) & 1)))) break;
+      l_buf[hh * kTcRows + r] = l;
+      if (hh == 0) m_buf[r] = m;
+      mbar_arrive(bar(kBarLReady));
+      ++ord;
     }
     if (!ok) fail();
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsEpilogue) : "memory");
-    // ====================== epilogue: one thread per row ======================
+    // ============ epilogue (and E4M3 converter): one thread per row ============
     const int r = tid & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int oc[2] = {0, 0};
+    const uint32_t tO = tmem + kTmO + lane_off;
+    int ord = 0;
     bool ok = true;
-    for (int k = 0; ok && k < nk; ++k) {
-      const Item it = item_of(p, seq_tab, k);
-      if (r == 0 && it.h == 0 && it.run == 0 && it.qp == p.n_qp - 1) {  // once per sequence
+    // the outputs of item k (or its split partials)
+    auto epilogue = [&](int k) -> bool {
+      const Item it = item_of(p, seq_tab, len_tab, tabs, k);
+      if (r == 0 && it.h == 0 && it.run == 0 && it.qt == p.n_qt - 1) {  // once per sequence
         const int L = __ldg(p.context_lens + it.s);
         if (L != it.L) atomicOr(p.err, kErrContextLen);  // negative, or past the table (or partitions)
       }
-      if (!it.valid) continue;
-      for (int i = 0; i < 2; ++i) {
-        if (it.ntok[i] == 0) continue;
-        const bool live = r < it.ntok[i] * p.G;
-        const int j = it.j0[i] + r / p.G;
-        const int64_t row = (static_cast<int64_t>(it.s) * p.C + j) * p.Hq + it.h * p.G + r % p.G;
-        const bool have = it.ntiles > 0;
-        float l = 0.f, m = -CUDART_INF_F;
+      if (!it.valid) return true;
+      const bool live = r < it.ntok * p.G;
+      const int j = it.j0 + r / p.G;
+      const int64_t row = (static_cast<int64_t>(it.s) * p.C + j) * p.Hq + it.h * p.G + r % p.G;
+      const bool have = it.ntiles > 0;
+      float l = 0.f, m = -CUDART_INF_F;
+      if (have) {
+        // the epilogue idles through most of an item: poll with a pause (at
+        // most about 50 ms) so that it takes few issue slots from the
+        // softmax warps, then the usual bounded wait
+        for (int spin = 0; spin < 400000 && !mbar_try_wait(bar(kBarOFull), ord & 1); ++spin) __nanosleep(128);
+        const bool got = !*abort_flag && __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFull), ord & 1)) &&
+                         __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarLReady), ord & 1));
+        if (!got) return false;
+        tc_fence_after();
+        l = l_buf[r] + l_buf[kTcRows + r];
+        m = m_buf[r];
+      }
+      const float inv = l > 0.f ? p.vscale / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
         if (have) {
-          // the epilogue idles through most of an item: poll with a pause (at
-          // most about 50 ms) so that it takes few issue slots from the
-          // softmax warps, then the usual bounded wait
-          for (int spin = 0; spin < 200000 && !mbar_try_wait(bar(kBarOFull + i), oc[i] & 1); ++spin)
-            __nanosleep(256);
-          ok = !*abort_flag && __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFull + i), oc[i] & 1)) &&
-               __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarLReady + i), oc[i] & 1));
-          if (!ok) break;
-          tc_fence_after();
-          l = l_buf[i * kTcRows + r];
-          m = m_buf[i * kTcRows + r];
-        }
-        const bool final_out = it.final_out;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        for (int c = 0; c < p.D / 32; ++c) {
-          float o[32];
-          if (have) {
-            tmem_ld32(tO(i) + lane_off + c * 32, o);
-            tmem_wait_ld();
-          } else {
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0.f;
-          }
-          if (!live) continue;
-          if (final_out) {
-            uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.D + c * 32;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv, p.bf16);
-              w.y = pack16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv, p.bf16);
-              w.z = pack16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv, p.bf16);
-              w.w = pack16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv, p.bf16);
-              *reinterpret_cast<uint4*>(orow + q4 * 8) = w;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.Pmax + it.run) * p.D + c * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-          }
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
         }
-        if (live && !final_out) {
-          const int64_t slot = row * p.Pmax + it.run;
-          p.ws_ml[2 * slot] = l > 0.f ? m : -CUDART_INF_F;
-          p.ws_ml[2 * slot + 1] = l;
-        }
-        if (have) {
-          // O_i and the (l, m) slot may take the next item's
+        if (c == D / 32 - 1 && have) {
+          // O and the (l, m) slots may take the next item's
           tc_fence_before();
-          mbar_arrive(bar(kBarOFree + i));
-          ++oc[i];
+          mbar_arrive(bar(kBarOFree));
+        }
+        if (!live) continue;
+        if (it.final_out) {
+          uint16_t* orow = static_cast<uint16_t*>(p.out) + row * D + c * 32;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv, p.out_bf16);
+            w.y = pack16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv, p.out_bf16);
+            w.z = pack16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv, p.out_bf16);
+            w.w = pack16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv, p.out_bf16);
+            *reinterpret_cast<uint4*>(orow + q4 * 8) = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.Pmax + it.run) * D + c * 32);
+          const float vs = p.vscale;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(o[4 * q4] * vs, o[4 * q4 + 1] * vs, o[4 * q4 + 2] * vs, o[4 * q4 + 3] * vs);
         }
       }
+      if (live && !it.final_out) {
+        const int64_t slot = row * p.Pmax + it.run;
+        p.ws_ml[2 * slot] = l > 0.f ? m : -CUDART_INF_F;
+        p.ws_ml[2 * slot + 1] = l;
+      }
+      if (have) ++ord;
+      return true;
+    };
+    if (!p.fp8) {
+      for (int k = 0; ok && k < nk; ++k) ok = epilogue(k);
+    } else {
+      // E4M3 caches: every ring load, in the order the producer issues them,
+      // is widened row by row (this thread: row r) from the 8-bit tile to the
+      // slot's 16-bit operand tile; rows past the tile's valid tokens become
+      // zeros (so 0 * junk cannot make NaN in P.V).  An item's outputs are
+      // written once the ring step holding its last V tile is widened.
+      // bf16 q with E4M3 caches: the MMA runs in f16, so row r of an item's
+      // query tile is scaled by 2^e with max|q| 2^e in [2^14, 2^15) and
+      // rounded to f16 in place (exact but for entries below 2^-29 max|q|);
+      // 2^-e goes to the softmax through qsc.  Done before the item's first K
+      // tile, in the producer's order, so it never waits on the softmax.
+      auto convert_q = [&](const Cursor& c) -> bool {
+        const int qb = c.ord & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQFull + qb), (c.ord >> 1) & 1))) return false;
+        float mul_inv = 1.f;
+        if (r < c.it.ntok * p.G) {
+          const uint32_t qrow = q_base + qb * TB + r * 128;
+          const int rsw = r & 7;
+          float qmax = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < D / 8; ++cc) {
+            const uint4 u = ld_shared_v4(qrow + (cc >> 3) * kHalfBytes + (((cc & 7) ^ rsw) << 4));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              qmax = fmaxf(qmax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+          }
+          int ex = 0, e2 = 0;
+          if (qmax > 0.f) {
+            frexpf(qmax, &ex);  // qmax = f 2^ex, f in [0.5, 1)
+            e2 = min(15 - ex, 126);
+          }
+          const float mul = ldexpf(1.f, e2);
+#pragma unroll
+          for (int cc = 0; cc < D / 8; ++cc) {
+            const uint32_t a = qrow + (cc >> 3) * kHalfBytes + (((cc & 7) ^ rsw) << 4);
+            const uint4 u = ld_shared_v4(a);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t hw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              hw[e] = pack16(__uint_as_float(w[e] << 16) * mul, __uint_as_float(w[e] & 0xFFFF0000u) * mul, 0);
+            st_shared_v4(a, hw[0], hw[1], hw[2], hw[3]);
+          }
+          mul_inv = ldexpf(1.f, -e2);
+        }
+        qsc[qb * kTcRows + r] = mul_inv;
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarQConv + qb));
+        return true;
+      };
+      int rslot = 0, rphase = 0;  // ring step: slot and phase parity
+      // one tile of a landed slot, widened in place (its half at s16)
+      auto convert = [&](const Cursor& c, uint32_t s16) {
+        const int valid = valid_tokens(c.it, c.t);
+        const uint32_t s8 = s16 + kStageOff;
+        const int rsw = r & 7;
+        if constexpr (D == 128) {
+          uint4 in[8];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            in[cc] = r < valid ? ld_shared_v4(s8 + r * 128 + ((cc ^ rsw) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {  // 16 channels: 16-bit chunks 2 cc, 2 cc + 1 of the row
+            uint32_t h[8];
+            e4m3x4_to_f16(in[cc].x, h[0], h[1]);
+            e4m3x4_to_f16(in[cc].y, h[2], h[3]);
+            e4m3x4_to_f16(in[cc].z, h[4], h[5]);
+            e4m3x4_to_f16(in[cc].w, h[6], h[7]);
+            const uint32_t rowa = s16 + (cc >> 2) * kHalfBytes + r * 128;
+            const int jj = 2 * (cc & 3);
+            st_shared_v4(rowa + ((jj ^ rsw) << 4), h[0], h[1], h[2], h[3]);
+            st_shared_v4(rowa + (((jj + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
+          }
+        } else {
+          uint4 in[4];
+          const int rsw64 = (r >> 1) & 3;  // 64-byte swizzle of the 8-bit rows
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            in[cc] = r < valid ? ld_shared_v4(s8 + r * 64 + ((cc ^ rsw64) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t h[8];
+            e4m3x4_to_f16(in[cc].x, h[0], h[1]);
+            e4m3x4_to_f16(in[cc].y, h[2], h[3]);
+            e4m3x4_to_f16(in[cc].z, h[4], h[5]);
+            e4m3x4_to_f16(in[cc].w, h[6], h[7]);
+            const uint32_t rowa = s16 + r * 128;
+            st_shared_v4(rowa + (((2 * cc) ^ rsw) << 4), h[0], h[1], h[2], h[3]);
+            st_shared_v4(rowa + (((2 * cc + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
+          }
+        }
+      };
+      // ring steps as the producer issues them: step 0 = K(0), K(1); step
+      // e >= 1 = V(e - 1), K(e + 1)
+      Cursor kc, vc;
+      cur_start(kc);
+      vc = kc;
+      int ke = 0;  // first item whose outputs are not yet written
+      auto step = [&](bool first) -> bool {
+        const int slot = rslot;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarSlotFull + slot), rphase))) return false;
+        const uint32_t dst = ring_base + slot * slot_b;
+        if (first) {
+          if (kc.t == 0 && p.q_scale_rows && !convert_q(kc)) return false;
+          convert(kc, dst);
+          cur_next(kc);
+        } else {
+          convert(vc, dst);
+          cur_next(vc);
+        }
+        if (kc.k < nk) {
+          if (kc.t == 0 && p.q_scale_rows && !convert_q(kc)) return false;
+          convert(kc, dst + half_b);
+          cur_next(kc);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarSlotConv + slot));
+        if (++rslot == p.nslot) {
+          rslot = 0;
+          rphase ^= 1;
+        }
+        return true;
+      };
+      if (kc.k < nk) ok = step(true);
+      while (ok && vc.k < nk) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const int vk = vc.k;
+        const bool item_done = vc.t == vc.it.ntiles - 1;
+        ok = step(false);
+        if (item_done)
+          for (; ok && ke <= vk; ++ke) ok = epilogue(ke);
+      }
+      for (; ok && ke < nk; ++ke) ok = epilogue(ke);
     }
     if (!ok) fail();
   }
@@ -727,35 +1028,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+template <int D>
+cudaError_t launch_d(const TcParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                     int grid, int smem, cudaStream_t st) {
+  // every warp role fits in the 128 registers a thread of the 512 gets
+  auto kern = attn_tc_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTcThreads, smem, st>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-int tc_ring_slots(int D, int NQ) {
-  const Layout L0 = layout_of(D, NQ, 0);
-  const int n = (kSmemLimit - L0.total) / tile_bytes(D);
+int tc_ring_slots(int D, int fp8) {
+  const Layout L0 = layout_of(D, 0, fp8);
+  const int n = (kSmemLimit - L0.total) / L0.slot;
   return n < kTcMaxSlots ? n : kTcMaxSlots;
 }
 
-int tc_smem_bytes(int D, int NQ, int nslot) { return layout_of(D, NQ, nslot).total; }
+int tc_smem_bytes(int D, int nslot, int fp8) { return layout_of(D, nslot, fp8).total; }
 
 cudaError_t launch_attn_tc(const TcParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            cudaStream_t st) {
-  if (p.nslot < 3 || p.nslot > kTcMaxSlots) return cudaErrorInvalidValue;
-  const int smem = tc_smem_bytes(p.D, p.NQ, p.nslot);
+  if (p.nslot < 2 || p.nslot > kTcMaxSlots || (p.D != 64 && p.D != 128)) return cudaErrorInvalidValue;
+  const int smem = tc_smem_bytes(p.D, p.nslot, p.fp8);
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  // the warpgroups' setmaxnreg shares must fit in the registers the CTA is
-  // launched with, or the softmax warps' increase would never be granted
-  static std::atomic<int> launch_regs{0};
-  int regs = launch_regs.load(std::memory_order_relaxed);
-  if (regs == 0) {
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_tc_kernel);
-    if (e != cudaSuccess) return e;
-    regs = fa.numRegs;
-    launch_regs.store(regs, std::memory_order_relaxed);
-  }
-  if (128 * (2 * kRegsSoftmax + kRegsEpilogue + kRegsAux) > regs * kTcThreads) return cudaErrorInvalidConfiguration;
   static std::atomic<int> sms[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
@@ -765,13 +1063,13 @@ cudaError_t launch_attn_tc(const TcParams& p, const CUtensorMap& tmQ, const CUte
     sms[dev].store(nsm, std::memory_order_relaxed);
   }
   if (p.total <= 0) return cudaSuccess;
-  // persistent: one CTA per SM (the kernel holds all of an SM's tensor memory)
+  // persistent: one CTA per SM (the kernel holds all of an SM's tensor memory,
+  // and its shared memory keeps a second CTA off the SM)
   const int grid = p.total < nsm ? p.total : nsm;
   TcParams q = p;
   // items per CTA beyond the table are not ordered
   if ((p.total + grid - 1) / grid > kTcMaxRanked) q.rank_seqs = 0;
-  attn_tc_kernel<<<grid, kTcThreads, smem, st>>>(tmQ, tmK, tmV, q);
-  return cudaGetLastError();
+  return p.D == 64 ? launch_d<64>(q, tmQ, tmK, tmV, grid, smem, st) : launch_d<128>(q, tmQ, tmK, tmV, grid, smem, st);
 }
 
 }  // namespace pa

@@ -60,7 +60,7 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
     lib.pa_decode_multi.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
                                     P]
-    lib.pa_prefill.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, P]
+    lib.pa_prefill.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
     lib.pa_prefill.restype = ctypes.c_int
     lib.pa_decode_split_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
@@ -233,7 +233,7 @@ def decode_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
 
 
 def prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float) -> None:
+            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float = 1.0) -> None:
     """Chunked prefill on the tensor cores: q/out [S, C, Hq, D] (D 64 or 128), causal over the paged context."""
     _check_caches(k_cache, v_cache)
     dev = k_cache.device
@@ -248,7 +248,7 @@ def prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     with torch.cuda.device(dev):
         rc = lib.pa_prefill(_ptr(out), _ptr(q), _dtype_code(q.dtype), S, C, Hq, _ptr(k_cache), _ptr(v_cache),
                             ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-                            float(scale), _stream(dev))
+                            float(scale), float(kv_scale), _stream(dev))
     _check("pa_prefill", rc)
 
 

@@ -70,10 +70,8 @@ def test_host_checks_return_codes_without_a_gpu(pa):
         assert L.pa_decode(FAKE, FAKE, 1, 1, 4, FAKE, FAKE, ctypes.byref(bad), FAKE, 4, FAKE, 0.1, 1.0, null) == -2
     # group of 256 query heads per kv head (above 128): unsupported; 5 % 2: invalid
     assert L.pa_decode(FAKE, FAKE, 1, 1, 512, FAKE, FAKE, ctypes.byref(d), FAKE, 4, FAKE, 0.1, 1.0, null) == -2
-    # a group of 32 goes to the tensor-core kernel, which takes scale > 0 and 16-bit caches
+    # a group of 32 goes to the tensor-core kernel, which takes scale > 0
     assert L.pa_decode(FAKE, FAKE, 1, 1, 64, FAKE, FAKE, ctypes.byref(d), FAKE, 4, FAKE, -0.1, 1.0, null) == -1
-    assert L.pa_decode(FAKE, FAKE, 1, 1, 64, FAKE, FAKE, ctypes.byref(_desc(pa, dt=2)), FAKE, 4, FAKE, 0.1, 1.0,
-                       null) == -2
     assert L.pa_decode(FAKE, FAKE, 1, 1, 5, FAKE, FAKE, ctypes.byref(d), FAKE, 4, FAKE, 0.1, 1.0, null) == -1
     # q dtype f16 with a bf16 cache
     assert L.pa_decode(FAKE, FAKE, 0, 1, 4, FAKE, FAKE, ctypes.byref(d), FAKE, 4, FAKE, 0.1, 1.0, null) == -2

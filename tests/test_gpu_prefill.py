@@ -148,10 +148,18 @@ def test_unsupported_and_invalid_arguments_launch_nothing():
     assert e.value.status == -2
     q = torch.zeros((1, 4, 2, 128), dtype=torch.bfloat16, device="cuda")
     k8 = torch.zeros((4, 2, 16, 128), dtype=torch.uint8, device="cuda")
-    with pytest.raises(pa.PagedAttnError) as e:  # FP8 caches: decode only
-        pa.prefill(q.clone(), q, k8, k8, bt, cl, 0.1)
+    for bad in (0.0, -2.0, float("inf")):  # FP8 caches need a positive finite kv_scale
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.prefill(q.clone(), q, k8, k8, bt, cl, 0.1, kv_scale=bad)
+        assert e.value.status == -1
+    f16 = torch.zeros((4, 2, 16, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:  # a 16-bit cache of another dtype than q
+        pa.prefill(q.clone(), q, f16, f16, bt, cl, 0.1)
     assert e.value.status == -2
     kc = torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:  # 16-bit caches take kv_scale 1
+        pa.prefill(q.clone(), q, kc, kc, bt, cl, 0.1, kv_scale=0.5)
+    assert e.value.status == -1
     for bad in (0.0, -1.0, float("nan")):
         with pytest.raises(pa.PagedAttnError) as e:
             pa.prefill(q.clone(), q, kc, kc, bt, cl, bad)

@@ -39,23 +39,46 @@ PREFILL = [
 ]
 
 
-@pytest.mark.parametrize("case", PREFILL, ids=lambda c: "Hq%d-Hkv%d-D%d-%s-bs%d-C%d" % c[:6])
-def test_prefill_packed_groups_and_head_dims(case):
-    Hq, Hkv, D, dt, bs, C, lens = case
-    wl = W.make_workload(name="t", seed=61, context_lens=lens, Hq=Hq, Hkv=Hkv, D=D, bs=bs, q_dtype=dt,
-                         kv_dtype=dt, qlen=C)
+def _prefill_case(Hq, Hkv, D, dt, bs, C, lens, kv_dtype=None, seed=61):
+    kd = dt if kv_dtype is None else kv_dtype
+    wl = W.make_workload(name="t", seed=seed, context_lens=lens, Hq=Hq, Hkv=Hkv, D=D, bs=bs, q_dtype=dt,
+                         kv_dtype=kd, qlen=C)
     pa = _gpu.lib()
     g = _gpu.OnGpu(wl)
     g.scatter()
     out = torch.full_like(g.q, float("nan"))
-    pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale)
+    pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale)
     torch.cuda.synchronize()
     assert pa.get_device_error() == 0
     kc, vc = _gpu.oracle_pool(wl)
-    assert _gpu.max_err(out, _gpu.oracle_out(wl, kc, vc)) <= _gpu.tolerance(wl)
+    gk, gv = g.caches_host()
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+    err = _gpu.max_err(out, _gpu.oracle_out(wl, kc, vc))
+    assert err <= _gpu.tolerance(wl), err
+    _check_zero_rows(out, wl)
     out2 = torch.full_like(g.q, float("nan"))
-    pa.prefill(out2, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale)
+    pa.prefill(out2, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale)
     assert torch.equal(out, out2)  # deterministic
+
+
+@pytest.mark.parametrize("case", PREFILL, ids=lambda c: "Hq%d-Hkv%d-D%d-%s-bs%d-C%d" % c[:6])
+def test_prefill_packed_groups_and_head_dims(case):
+    _prefill_case(*case)
+
+
+PREFILL_FP8 = [
+    # (Hq, Hkv, D, q dtype, bs, C, context lengths): E4M3 caches with a per-tensor scale
+    (32, 8, 128, "bf16", 16, 256, [256, 300, 1000, 129]),
+    (8, 2, 64, "bf16", 16, 200, [200, 777]),
+    (4, 4, 128, "f16", 8, 150, [150, 151, 600]),
+    (12, 4, 64, "f16", 32, 90, [90, 400, 1100]),
+    (64, 8, 128, "bf16", 16, 40, [40, 2100]),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_FP8, ids=lambda c: "Hq%d-Hkv%d-D%d-%s-bs%d-C%d-fp8" % c[:6])
+def test_prefill_fp8_caches(case):
+    _prefill_case(*case, kv_dtype="fp8", seed=65)
 
 
 WIDE = [
@@ -68,25 +91,28 @@ WIDE = [
     (16, 8, 64, "bf16", 16),    # G = 2, 16 tokens: 32 columns
     (256, 2, 64, "bf16", 1),    # G = 128
 ]
+WIDE_FP8 = [
+    # (Hq, Hkv, D, q dtype, k): E4M3 caches
+    (32, 8, 128, "bf16", 8),
+    (64, 8, 128, "bf16", 4),
+    (16, 4, 64, "f16", 6),
+]
 
 
 def _wide_id(c):
     return "Hq%d-Hkv%d-D%d-%s-k%d" % c
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two"])
-@pytest.mark.parametrize("P", [0, 64, 512])
-@pytest.mark.parametrize("case", WIDE, ids=_wide_id)
-def test_wide_group_decode(case, P, fused):
+def _wide_case(case, P, fused, kv_dtype=None):
     Hq, Hkv, D, dt, k = case
     wl = W.make_workload(name="t", seed=62, context_lens=LENS, Hq=Hq, Hkv=Hkv, D=D, bs=16, q_dtype=dt,
-                         kv_dtype=dt, qlen=k)
+                         kv_dtype=dt if kv_dtype is None else kv_dtype, qlen=k)
     pa = _gpu.lib()
     assert pa.get_device_error() == 0
     g = _gpu.OnGpu(wl)
     if fused:
         out = torch.full_like(g.q, float("nan"))
-        pa.cache_and_decode(out, g.q, g.key, g.value, g.slots, g.kc, g.vc, g.bt, g.cl, wl.scale,
+        pa.cache_and_decode(out, g.q, g.key, g.value, g.slots, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale,
                             max_context_len=wl.max_context_len, partition_size=P)
     else:
         out = g.step(partition_size=P).clone()
@@ -101,6 +127,20 @@ def test_wide_group_decode(case, P, fused):
     assert torch.equal(g.decode(partition_size=P), out)  # deterministic
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two"])
+@pytest.mark.parametrize("P", [0, 64, 512])
+@pytest.mark.parametrize("case", WIDE, ids=_wide_id)
+def test_wide_group_decode(case, P, fused):
+    _wide_case(case, P, fused)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two"])
+@pytest.mark.parametrize("P", [0, 128])
+@pytest.mark.parametrize("case", WIDE_FP8, ids=lambda c: _wide_id(c) + "-fp8")
+def test_wide_group_decode_fp8(case, P, fused):
+    _wide_case(case, P, fused, kv_dtype="fp8")
+
+
 def _draw(i):
     rng = np.random.default_rng(5000 + i)
     while True:
@@ -110,8 +150,9 @@ def _draw(i):
         if 16 < G * k <= 160:
             break
     dt = ["f16", "bf16"][int(rng.integers(0, 2))]
+    kd = dt if rng.integers(0, 3) else "fp8"
     S = int(rng.integers(1, 6))
-    return dict(Hq=G * Hkv, Hkv=Hkv, D=int(rng.choice([64, 128])), bs=int(rng.choice([8, 16, 32])), dt=dt, k=k,
+    return dict(Hq=G * Hkv, Hkv=Hkv, D=int(rng.choice([64, 128])), bs=int(rng.choice([8, 16, 32])), dt=dt, kd=kd, k=k,
                 lens=[int(x) for x in rng.integers(1, 2500, size=S)], P=int(rng.choice([0, 64, 128, 512])),
                 fused=bool(rng.integers(0, 2)), seed=6000 + i)
 
@@ -119,18 +160,19 @@ def _draw(i):
 SWEEP = [_draw(i) for i in range(24)]
 
 
-@pytest.mark.parametrize("c", SWEEP, ids=lambda c: "Hq%d-Hkv%d-D%d-bs%d-%s-k%d-P%d-%s" % (
-    c["Hq"], c["Hkv"], c["D"], c["bs"], c["dt"], c["k"], c["P"], "fused" if c["fused"] else "two"))
+@pytest.mark.parametrize("c", SWEEP, ids=lambda c: "Hq%d-Hkv%d-D%d-bs%d-%s-%s-k%d-P%d-%s" % (
+    c["Hq"], c["Hkv"], c["D"], c["bs"], c["dt"], c["kd"], c["k"], c["P"], "fused" if c["fused"] else "two"))
 def test_wide_group_sweep(c):
     """Seeded draws of group size (1-32), new tokens (1-16, G x k from 17 to
-    160 columns), head_dim, block size, dtype, partition size and launch form."""
+    160 columns), head_dim, block size, q and cache dtype (a third E4M3),
+    partition size and launch form."""
     wl = W.make_workload(name="t", seed=c["seed"], context_lens=c["lens"], Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"],
-                         bs=c["bs"], q_dtype=c["dt"], kv_dtype=c["dt"], qlen=c["k"])
+                         bs=c["bs"], q_dtype=c["dt"], kv_dtype=c["kd"], qlen=c["k"])
     pa = _gpu.lib()
     g = _gpu.OnGpu(wl)
     if c["fused"]:
         out = torch.full_like(g.q, float("nan"))
-        pa.cache_and_decode(out, g.q, g.key, g.value, g.slots, g.kc, g.vc, g.bt, g.cl, wl.scale,
+        pa.cache_and_decode(out, g.q, g.key, g.value, g.slots, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale,
                             max_context_len=wl.max_context_len, partition_size=c["P"])
     else:
         out = g.step(partition_size=c["P"]).clone()
