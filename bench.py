@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences (profiling runs)")
     ap.add_argument("--qlen", type=int, default=1, help="new query tokens per sequence (multi-token decode)")
     ap.add_argument("--block-size", type=int, default=16, help="KV block size of the prefill workload (8, 16, 32)")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache dtype of the prefill workload")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128], help="head_dim of the prefill workload")
     ap.add_argument("--op", default="decode", choices=["decode", "blocks", "prefill"],
                     help="blocks: time copy-on-write block copies and swap-out/in through pinned host memory")
     ap.add_argument("--ref-budget", type=float, default=0.0,
@@ -201,7 +203,10 @@ DECODE_SOURCES = ("pa_decode.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_decode_f16
                   "pa_decode_fp8.cu")
 
 
-PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
+TC_SOURCES = ("pa_attn_tc.cu", "pa_attn_tc.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
+
+
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill.h") + TC_SOURCES
 
 
 def kernel_source_hash(sources=DECODE_SOURCES) -> str:
@@ -234,17 +239,18 @@ def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch recorded by an ncu capture under profiles/, valid
     only while the kernel sources hash to the value recorded with it."""
     try:
-        return float(_profile_values("%s_%s" % (kernel, workload), DECODE_SOURCES)["dram_bytes_per_launch_full_size"])
+        sources = TC_SOURCES if kernel.startswith("attn_tc") else DECODE_SOURCES
+        return float(_profile_values("%s_%s" % (kernel, workload), sources)["dram_bytes_per_launch_full_size"])
     except (KeyError, ValueError):
         return None
 
 
-def recorded_prefill_traffic(chunk: int, seqs: int):
+def recorded_prefill_traffic(name: str, chunk: int, seqs: int):
     """DRAM bytes of one prefill launch over `seqs` sequences with a `chunk`-token
     chunk at context 2 x chunk: the captured bytes per sequence (every
     sequence reads its own q, K and V and writes its own output) times seqs."""
     try:
-        per_seq = float(_profile_values("prefill_gqa8b_chunk%d" % chunk, PREFILL_SOURCES)["dram_bytes_per_sequence"])
+        per_seq = float(_profile_values("%s_chunk%d" % (name, chunk), PREFILL_SOURCES)["dram_bytes_per_sequence"])
     except (KeyError, ValueError):
         return None
     return per_seq * seqs
@@ -602,9 +608,10 @@ def run_prefill(args, local):
     """Chunked prefill of a GQA 8B-shaped batch through pa_prefill: by default
     16 sequences, each with a chunk of 2048 new tokens at the end of a
     4096-token context (32/8 heads, head_dim 128, bf16, block size 16);
-    --seqs and --qlen change the batch and the chunk (context = 2 x chunk).
-    TFLOP/s counts the causal work only: 4 * D * Hq * sum over query rows of
-    (position + 1)."""
+    --seqs and --qlen change the batch and the chunk (context = 2 x chunk),
+    --kv-dtype fp8 stores the caches in E4M3 (per-tensor scale) and
+    --head-dim 64 halves the head.  TFLOP/s counts the causal work only:
+    4 * D * Hq * sum over query rows of (position + 1)."""
     import torch
     from paged_kv_cache_230_gb300 import build as _build
     _build.build()
@@ -615,13 +622,14 @@ def run_prefill(args, local):
     C = args.qlen if args.qlen > 1 else 2048
     L = 2 * C
     bs = getattr(args, "block_size", 16)
-    wl = W.make_prefill_workload(S=S, C=C, bs=bs)
+    kv = W.FP8 if getattr(args, "kv_dtype", "bf16") == "fp8" else W.BF16
+    wl = W.make_prefill_workload(S=S, C=C, bs=bs, kv_dtype=kv, D=getattr(args, "head_dim", 128))
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
     flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())
 
     def run():
-        pa.prefill(b.out, b.q, b.k_cache, b.v_cache, b.block_tables, b.context_lens, wl.scale)
+        pa.prefill(b.out, b.q, b.k_cache, b.v_cache, b.block_tables, b.context_lens, wl.scale, wl.kv_scale)
 
     for _ in range(max(3, args.warmup)):
         run()
@@ -658,13 +666,16 @@ def run_prefill(args, local):
     peak, kind = measured_tensor_peak(sustained=True)
     burst, _ = measured_tensor_peak()
     line = {"metric": "paged prefill attention TFLOP/s (causal FLOPs)", "value": tflops, "unit": "TFLOP/s",
-            "n_gpus": 1, "steps": K, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "n_gpus": 1, "steps": K, "warmup": args.warmup, "higher_is_better": True,
+            # E4M3 tiles are widened to f16 in shared memory: the MMAs run in f16
+            "dtype": "f16" if kv == W.FP8 else "bf16",
             "data": "synthetic", "config": {"workload": wl.name, "num_seqs": S, "chunk": C, "context": L,
-                                            "q_heads": 32, "kv_heads": 8, "head_dim": 128, "block_size": bs},
+                                            "q_heads": 32, "kv_heads": 8, "head_dim": wl.D, "block_size": bs,
+                                            "kv_dtype": wl.kv_dtype},
             "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6), "clocks": clocks,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "peak_source": kind, "frac_of_burst_peak": tflops / burst,
-                         "traffic": recorded_prefill_traffic(C, S), "kernel": "pa_prefill"}}
+                         "traffic": recorded_prefill_traffic(wl.name, C, S), "kernel": "pa_prefill"}}
     print(json.dumps(line), flush=True)
 
 

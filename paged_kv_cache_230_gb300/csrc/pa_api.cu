@@ -332,7 +332,8 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
   p.partition_size = partition_size > 0 ? partition_size : 0;
   p.Pmax = static_cast<int>(Pmax);
   p.ppc = static_cast<int>(ppc);
-  p.nslot = pa::tc_ring_slots(D, fp8);
+  p.nqb = 2;
+  p.nslot = pa::tc_ring_slots(D, fp8, p.nqb);
   p.rank_seqs = 1;
   p.out_bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
   // E4M3 caches are widened to f16 (exact), so the MMA runs in f16; bf16 q

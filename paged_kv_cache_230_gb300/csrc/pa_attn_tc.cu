@@ -14,13 +14,14 @@
 // c + grid, ...; items ordered by context length, longest first, then kv
 // head, last query tiles first, then runs of partitions in the split
 // variant).  Tensor memory holds two score buffers S (128 columns each), two
-// probability buffers P (64 columns each: 16-bit pairs) and the output O, so
-// the tensor core never waits on its own results: while the softmax works on
-// tile g, one issuing thread runs O += P(g - 1) V(g - 1) interleaved MMA by
-// MMA with S(g + 1) = Q K(g + 1)^T, two accumulators in flight (a chain of
-// MMAs into one accumulator waits on itself and runs at about half rate).
-// P.V takes its A operand from tensor memory, so shared memory only feeds Q,
-// K and V.  16 warps in four warpgroups:
+// probability buffers P (64 columns each: 16-bit pairs) and the output O.
+// Two threads issue the MMAs: one runs S(j) = Q K(j)^T as soon as K(j) has
+// landed and the softmax has read S(j - 2) out of its buffer, the other
+// O += P(j) V(j) once the softmax has written P(j); their MMAs meet on the
+// tensor core in alternation, two accumulators in flight (a chain of MMAs
+// into one accumulator waits on itself), and each thread's waits overlap
+// the other's MMAs.  P.V takes its A operand from tensor memory, so shared
+// memory only feeds Q, K and V.  16 warps:
 //   warps 0-3, 4-7  softmax: one thread per (row, column half): tcgen05.ld of
 //       64 scores, causal mask where a tile crosses the row's position, the
 //       row max combined with the other half's through shared memory, online
@@ -30,15 +31,10 @@
 //       unnormalised partial and its (m, l) to the split workspace); with
 //       E4M3 caches also the converter that widens each 8-bit K/V tile to
 //       16 bits in shared memory (and rounds bf16 q to f16);
-//   warps 12, 14, 15  TMA: each item's query tile (two buffers), then
-//       128-token K and V tiles block by block through the block table into a
-//       ring of slots, in the order the tensor core consumes them: a slot
-//       holds the two tiles one MMA phase reads, V(g) and K(g + 2), behind
-//       one barrier; a warp waits about 130 cycles on each box it issues, so
-//       the boxes are spread over three warps (warp 12 arms the byte count);
-//   warp 13     the MMA issuer: per phase it waits for one ring slot and one
-//       P buffer, issues 16 MMAs, and commits one barrier that tells the
-//       softmax both that S(g + 2) is ready and that P buffer g & 1 is free.
+//   warp 12     TMA: each item's query tile (two buffers) and the 128-token K
+//       tiles, block by block through the block table, into the K ring;
+//   warp 15     TMA: the V tiles into the V ring;
+//   warp 13     the Q.K^T issuer; warp 14 the P.V issuer.
 // Every mbarrier wait gives up after about one second (error bit); a warp
 // that gives up raises a shared abort flag that stops the others, and
 // in-flight MMAs and TMA loads are drained (bounded) before the tensor
@@ -64,20 +60,18 @@ constexpr int kErrLayout = 0x10;
 
 constexpr int kHalfBytes = kTcRows * 128;  // 64 channels (128 bytes) of 128 rows
 constexpr int kStageOff = kHalfBytes;      // E4M3 tile inside a ring slot (see slot_bytes)
-constexpr int kProdWarp = 12, kMmaWarp = 13;  // warps 14, 15 issue TMA boxes too
-constexpr int kProdWarps = 3;
+constexpr int kKProdWarp = 12, kSWarp = 13, kPvWarp = 14, kVProdWarp = 15;
 // tensor memory columns
 constexpr uint32_t kTmS = 0, kTmP = 256, kTmO = 384;
-// mbarriers (8 bytes each): q full / empty / converted per q buffer; phase
-// done, P full and max exchange per score buffer; O full / free and l ready;
-// full / empty / converted per ring slot; drain.  "Phase done" b completes
-// when the MMAs of a phase finish: those of phase e (P.V(e) and S(e + 2), or
-// S(e + 2) alone for e = -2, -1) complete barrier (e & 1) for the
-// ((e + 2) >> 1)-th time.
-constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarQConv = 4, kBarPh = 6, kBarPFull = 8, kBarXchg = 10,
-              kBarOFull = 12, kBarOFree = 13, kBarLReady = 14, kBarSlotFull = 15,
-              kBarSlotEmpty = kBarSlotFull + kTcMaxSlots, kBarSlotConv = kBarSlotEmpty + kTcMaxSlots,
-              kBarDrain = kBarSlotConv + kTcMaxSlots, kNumBars = kBarDrain + 1;
+// mbarriers (8 bytes each): q full / empty / converted per q buffer; S full
+// / free, P full, P.V done and max exchange per score buffer; O full / free
+// and l ready; full / empty / converted per K slot and per V slot; one drain
+// barrier per issuer
+constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarQConv = 4, kBarSFull = 6, kBarSFree = 8, kBarPFull = 10,
+              kBarPvDone = 12, kBarXchg = 14, kBarOFull = 16, kBarOFree = 17, kBarLReady = 18,
+              kBarKFull = 19, kBarKEmpty = kBarKFull + kTcMaxSlots, kBarKConv = kBarKEmpty + kTcMaxSlots,
+              kBarVFull = kBarKConv + kTcMaxSlots, kBarVEmpty = kBarVFull + kTcMaxSlots,
+              kBarVConv = kBarVEmpty + kTcMaxSlots, kBarDrain = kBarVConv + kTcMaxSlots, kNumBars = kBarDrain + 2;
 // after the barriers: abort flag, TMEM address, this CTA's item -> sequence
 // and context-length tables, the row-max exchange [2][2][128], the row sums
 // [2][128] and reference maxima [128] handed to the epilogue, and the rows' q
@@ -96,28 +90,31 @@ constexpr float kRescaleThreshold = 8.f;
 
 __host__ __device__ constexpr int tile_bytes(int D) { return kTcRows * D * 2; }
 
-// A ring slot holds two tiles (V(g), then K(g + 2)); each half holds one
-// 16-bit K or V tile in the MMA's operand layout.  With E4M3 caches the TMA
-// lands the 8-bit tile at kStageOff of its half and the converter widens it
-// there: for head_dim 128 in place (the 8-bit row r sits where the second
-// channel half of 16-bit row r goes, and only the thread that owns row r
-// touches either), for head_dim 64 in an extra 8 KB behind the 16-bit tile.
-__host__ __device__ constexpr int half_bytes(int D, int fp8) {
+// A ring slot holds one 16-bit K or V tile in the MMA's operand layout.
+// With E4M3 caches the TMA lands the 8-bit tile at kStageOff and the
+// converter widens it there: for head_dim 128 in place (the 8-bit row r sits
+// where the second channel half of 16-bit row r goes, and only the thread
+// that owns row r touches either), for head_dim 64 in an extra 8 KB behind
+// the 16-bit tile.
+__host__ __device__ constexpr int slot_bytes(int D, int fp8) {
   return (fp8 && D == 64) ? tile_bytes(D) + kTcRows * 64 : tile_bytes(D);
 }
-__host__ __device__ constexpr int slot_bytes(int D, int fp8) { return 2 * half_bytes(D, fp8); }
 
 struct Layout {
-  int q, ring, slot, tail, total;
+  int q, kring, vring, slot, nks, nvs, tail, total;
 };
 
-// two q buffers (one per item parity), the ring, the tail
-__host__ __device__ inline Layout layout_of(int D, int nslot, int fp8) {
+// nqb q buffers (items alternate between two, or share one), the K ring
+// (the first half of the slots, rounded up), the V ring, the tail
+__host__ __device__ inline Layout layout_of(int D, int nslot, int fp8, int nqb) {
   Layout L;
   L.q = 0;
-  L.ring = 2 * tile_bytes(D);
   L.slot = slot_bytes(D, fp8);
-  L.tail = L.ring + nslot * L.slot;
+  L.nks = (nslot + 1) / 2;
+  L.nvs = nslot / 2;
+  L.kring = nqb * tile_bytes(D);
+  L.vring = L.kring + L.nks * L.slot;
+  L.tail = L.vring + L.nvs * L.slot;
   L.total = L.tail + kTailBytes;
   return L;
 }
@@ -277,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) atomicOr(p.err, kErrLayout);
     return;
   }
-  const Layout Ly = layout_of(D, p.nslot, p.fp8);
+  const Layout Ly = layout_of(D, p.nslot, p.fp8, p.nqb);
   const uint32_t bar0 = base + Ly.tail;
   auto bar = [&](int k) -> uint32_t { return bar0 + 8u * k; };
   uint8_t* tail = smem + Ly.tail;
@@ -289,38 +286,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* l_buf = reinterpret_cast<float*>(tail + kLOff);    // [2 halves][128]
   float* m_buf = reinterpret_cast<float*>(tail + kMOff);    // [128]
   float* qsc = reinterpret_cast<float*>(tail + kQscOff);    // [2 q buffers][128]
-  const uint32_t q_base = base + Ly.q, ring_base = base + Ly.ring;
-  const int slot_b = Ly.slot, half_b = half_bytes(D, p.fp8);
+  const uint32_t q_base = base + Ly.q, kring = base + Ly.kring, vring = base + Ly.vring;
+  const int slot_b = Ly.slot;
   const int nk = (p.total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                  static_cast<int>(gridDim.x);  // this CTA's work items
   const bool tabs = nk <= kTcMaxRanked;
+  // the q buffer of the item with ordinal o among those with tiles, and the
+  // parity of that buffer's phase for it
+  const bool q2 = p.nqb == 2;
+  auto q_buf = [q2](int o) { return q2 ? (o & 1) : 0; };
+  auto q_par = [q2](int o) { return (q2 ? o >> 1 : o) & 1; };
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarQFull + i), 1);
-      mbar_init(bar(kBarQEmpty + i), 1);
+      mbar_init(bar(kBarQEmpty + i), p.q_scale_rows ? 1 + 2 * kTcRows : 1);
       mbar_init(bar(kBarQConv + i), kTcRows);
-      mbar_init(bar(kBarPh + i), 1);
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSFree + i), 2 * kTcRows);
       mbar_init(bar(kBarPFull + i), 2 * kTcRows);
+      mbar_init(bar(kBarPvDone + i), 1);
       mbar_init(bar(kBarXchg + i), 2 * kTcRows);
+      mbar_init(bar(kBarDrain + i), 1);
     }
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarOFree), kTcRows);
     mbar_init(bar(kBarLReady), 2 * kTcRows);
-    for (int k = 0; k < p.nslot; ++k) {
-      mbar_init(bar(kBarSlotFull + k), 1);
-      mbar_init(bar(kBarSlotEmpty + k), 1);
-      mbar_init(bar(kBarSlotConv + k), kTcRows);
+    for (int k = 0; k < kTcMaxSlots; ++k) {
+      mbar_init(bar(kBarKFull + k), 1);
+      mbar_init(bar(kBarKEmpty + k), 1);
+      mbar_init(bar(kBarKConv + k), kTcRows);
+      mbar_init(bar(kBarVFull + k), 1);
+      mbar_init(bar(kBarVEmpty + k), 1);
+      mbar_init(bar(kBarVConv + k), kTcRows);
     }
-    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   // Longest-first order: the sequence of each of this CTA's items, from a
-  // histogram of context-length buckets built in the (not yet used) ring;
+  // histogram of context-length buckets built in the (not yet used) K ring;
   // then the items' context lengths.
   if (tabs && p.rank_seqs) {
-    int* hist = reinterpret_cast<int*>(smem + Ly.ring);  // [128] counts, then [128] offsets
+    int* hist = reinterpret_cast<int*>(smem + Ly.kring);  // [128] counts, then [128] offsets
     int* offs = hist + 128;
     if (tid < 128) hist[tid] = 0;
     __syncthreads();
@@ -386,7 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     for (int k = tid; k < nk; k += kTcThreads) len_tab[k] = __ldg(p.context_lens + seq_tab[k]);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -422,276 +429,205 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // tokens of KV tile t of an item that lie in its range
   auto valid_tokens = [](const Item& it, int t) { return min(kTcTok, it.kv_hi - (it.kv_lo + t * kTcTok)); };
 
-  if (warp >= 12) {
-    if (warp != kMmaWarp) {
-      // ============================ TMA producers ============================
-      // producer w issues the boxes i = w, w + 3, ... of each tile: box i is
-      // 64-channel half i % HALVES of block i / HALVES (one box per block
-      // for E4M3); this lane's box is i = 3 lane + w
-      const int w = warp == kProdWarp ? 0 : warp - 13;
-      const bool lead = w == 0;  // arms the byte counts and loads the query tiles
-      const int bpb = p.fp8 ? 1 : HALVES;  // boxes per block
-      const int my_box = kProdWarps * lane + w;
-      const int my_blk = my_box / bpb, my_half = my_box % bpb;
-      int rslot = 0, rphase = 0, n = 0;  // ring step n: its slot and phase parity
-      if (lead && lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
+  if (warp == kKProdWarp || warp == kVProdWarp) {
+    // ============================ TMA producers ============================
+    // warp 12: the query tiles and the K tiles; warp 15: the V tiles.  Lane i
+    // issues box i of a tile: 64-channel half i % HALVES of block i / HALVES
+    // (one box of D bytes per block for E4M3); a tile has at most
+    // 128 / 8 blocks x 2 halves = 32 boxes.
+    const bool is_k = warp == kKProdWarp;
+    const CUtensorMap* map = is_k ? &tmK : &tmV;
+    const int bpb = p.fp8 ? 1 : HALVES;  // boxes per block
+    const int my_blk = lane / bpb, my_half = lane % bpb;
+    const int nslots = is_k ? Ly.nks : Ly.nvs;
+    const uint32_t ring = is_k ? kring : vring;
+    const int full_bar = is_k ? kBarKFull : kBarVFull, empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
+    if (lane == 0) {
+      tma_prefetch_desc(map);
+      if (is_k) tma_prefetch_desc(&tmQ);
+    }
+    // blocks of a tile: at most 128 / 8 = 16
+    auto tile_blocks = [&](const Cursor& c, int& b0) -> int {
+      const int tok0 = c.it.kv_lo + c.t * kTcTok;
+      b0 = tok0 / p.bs;
+      return (tok0 + valid_tokens(c.it, c.t) - 1) / p.bs - b0 + 1;
+    };
+    // the block id of this lane's box, read one tile ahead of the load that
+    // needs it (the block-table read is a dependent global load)
+    auto tile_id = [&](const Cursor& c) -> int {
+      if (c.k >= nk) return -1;
+      int b0;
+      const int nb = tile_blocks(c, b0);
+      return my_blk < nb ? __ldg(p.block_tables + static_cast<int64_t>(c.it.s) * p.maxB + b0 + my_blk) : -1;
+    };
+    int rslot = 0, rphase = 0, n = 0, nq = 0;  // ring step n: its slot and phase parity; q tiles loaded
+    bool ok = true;
+    Cursor c;
+    cur_start(c);
+    int pre = tile_id(c);
+    while (c.k < nk) {
+      if (*abort_flag) {
+        ok = false;
+        break;
       }
-      bool ok = true;
-      // blocks of a tile: at most 128 / 8 = 16
-      auto tile_blocks = [&](const Cursor& c, int& b0) -> int {
-        const int tok0 = c.it.kv_lo + c.t * kTcTok;
-        b0 = tok0 / p.bs;
-        return (tok0 + valid_tokens(c.it, c.t) - 1) / p.bs - b0 + 1;
-      };
-      // the block id of this lane's box in the cursor's tile, read ahead of
-      // the load that needs it (the block-table read is a dependent global load)
-      auto tile_id = [&](const Cursor& c) -> int {
-        if (c.k >= nk) return -1;
-        int b0;
-        const int nb = tile_blocks(c, b0);
-        return my_blk < nb ? __ldg(p.block_tables + static_cast<int64_t>(c.it.s) * p.maxB + b0 + my_blk) : -1;
-      };
-      auto tile_bytes_of = [&](const Cursor& c) -> uint32_t {
-        int b0;
-        return static_cast<uint32_t>(tile_blocks(c, b0) * p.bs * D * (p.fp8 ? 1 : 2));
-      };
-      // this lane's box of a K or V tile into half `hf2` of the step's slot
-      auto issue_tile = [&](const Cursor& c, bool is_v, int phys, uint32_t dst, uint32_t full) {
-        int b0;
-        const int nb = tile_blocks(c, b0);
-        if (my_blk < nb) {
-          if (!is_v && my_half == 0 && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks))
-            atomicOr(p.err, kErrBlockId);
-          if (p.fp8)  // one box of D bytes per row: the 8-bit tile, widened later
-            tma_load_4d(dst + kStageOff + my_blk * p.bs * D, is_v ? &tmV : &tmK, full, 0, 0, c.it.h, phys);
-          else
-            tma_load_4d(dst + my_blk * p.bs * 128 + my_half * kHalfBytes, is_v ? &tmV : &tmK, full, 64 * my_half, 0,
-                        c.it.h, phys);
-        }
-      };
-      // an item's query tile (G heads x T tokens per 64-channel half) into q
-      // buffer ord & 1, once the item two before it has finished with it
-      int nq = 0;  // query tiles loaded
-      auto load_q = [&](const Cursor& c) -> bool {
-        ++nq;
-        if (!lead) return true;
-        const int qb = c.ord & 1;
-        if (c.ord >= 2 && !mbar_wait(bar(kBarQEmpty + qb), ((c.ord - 2) >> 1) & 1)) return false;
+      if (is_k && c.t == 0) {
+        // the item's query tile (G heads x T tokens per 64-channel half) into
+        // its q buffer, once the item that used the buffer before has finished
+        // with it
+        const int qb = q_buf(c.ord);
+        if (c.ord >= p.nqb &&
+            !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQEmpty + qb), q_par(c.ord - p.nqb)))))
+          break;
         if (lane == 0) {
           const uint32_t full = bar(kBarQFull + qb);
           mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.G * p.T * 128 * HALVES));
 #pragma unroll
           for (int hf = 0; hf < HALVES; ++hf)
-            tma_load_3d(q_base + qb * TB + hf * kHalfBytes, &tmQ, full, 64 * hf, c.it.h * p.G,
-                        c.it.s * p.C + c.it.j0);
-        }
-        __syncwarp();
-        return true;
-      };
-      // ring steps in the tensor core's order: step 0 = K(0), K(1); step
-      // e >= 1 = V(e - 1), K(e + 1).  V(g) reuses the block ids read for K(g):
-      // ids of the K tiles whose V is still to come wait in f0 (oldest), f1;
-      // the next K tile's ids are read as soon as the previous K is issued.
-      Cursor kc, vc;
-      cur_start(kc);
-      vc = kc;
-      int pre = tile_id(kc), f0 = -1, f1 = -1, nf = 0;
-      // one step: tile a (a V, or K(0) at step 0) into the first half, K of the
-      // K cursor (if any) into the second
-      auto step = [&](bool first) -> bool {
-        const int slot = rslot;
-        if (n >= p.nslot && !mbar_wait(bar(kBarSlotEmpty + slot), rphase ^ 1)) return false;
-        const uint32_t dst = ring_base + slot * slot_b, full = bar(kBarSlotFull + slot);
-        // tile a
-        Cursor ca = first ? kc : vc;
-        int ida;
-        if (first) {
-          if (kc.t == 0 && !load_q(kc)) return false;
-          ida = pre;
-          f0 = ida;
-          nf = 1;
-          cur_next(kc);
-          pre = tile_id(kc);
-        } else {
-          ida = f0;
-          f0 = f1;
-          --nf;
-          cur_next(vc);
-        }
-        // tile b: the next K, if there is one
-        const bool has_b = kc.k < nk;
-        Cursor cb = kc;
-        int idb = -1;
-        if (has_b) {
-          if (kc.t == 0 && !load_q(kc)) return false;
-          idb = pre;
-          if (nf == 0) f0 = idb; else f1 = idb;
-          ++nf;
-          cur_next(kc);
-          pre = tile_id(kc);
-        }
-        // the byte count may be armed after another producer's boxes have
-        // landed: the transaction count goes negative until then, and the
-        // phase cannot complete before the arrival that arms it
-        if (lead && lane == 0)
-          mbar_arrive_expect_tx(full, tile_bytes_of(ca) + (has_b ? tile_bytes_of(cb) : 0u));
-        __syncwarp();
-        issue_tile(ca, !first, ida, dst, full);
-        if (has_b) issue_tile(cb, false, idb, dst + half_b, full);
-        __syncwarp();
-        ++n;
-        if (++rslot == p.nslot) {
-          rslot = 0;
-          rphase ^= 1;
-        }
-        return true;
-      };
-      if (kc.k < nk) ok = step(true);
-      while (ok && vc.k < nk) {
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        if (vc.t == 0 && lead && lane == 0) {  // the query tile of the item after next into L2 ahead of time
+            tma_load_3d(q_base + qb * TB + hf * kHalfBytes, &tmQ, full, 64 * hf, c.it.h * p.G, c.it.s * p.C + c.it.j0);
+          // the next item's query tile into L2 ahead of time
           Item nx;
-          if (next_active(vc.k + 1, nx) < nk)
+          if (next_active(c.k + 1, nx) < nk)
             for (int hf = 0; hf < HALVES; ++hf) tma_prefetch_3d(&tmQ, 64 * hf, nx.h * p.G, nx.s * p.C + nx.j0);
         }
-        ok = step(false);
+        ++nq;
+        __syncwarp();
       }
-      if (!ok) fail();
-      // every load issued lands before the CTA can exit (the lead producer
-      // armed every slot whose boxes any producer issued, so the last nslot
-      // phases complete once all those boxes land)
-      for (int u = max(0, n - p.nslot); u < n; ++u) mbar_wait(bar(kBarSlotFull + u % p.nslot), (u / p.nslot) & 1);
-      if (lead)
-        for (int u = max(0, nq - 2); u < nq; ++u) mbar_wait(bar(kBarQFull + (u & 1)), (u >> 1) & 1);
-    } else if (warp == kMmaWarp) {
-      // ============================= MMA issuer =============================
+      if (n >= nslots && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(empty_bar + rslot), rphase ^ 1)))) break;
+      const uint32_t full = bar(full_bar + rslot), dst = ring + rslot * slot_b;
+      int b0;
+      const int nb = tile_blocks(c, b0);
+      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * p.bs * D * (p.fp8 ? 1 : 2)));
+      __syncwarp();
+      if (my_blk < nb) {
+        const int phys = pre;
+        if (is_k && my_half == 0 && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks))
+          atomicOr(p.err, kErrBlockId);
+        if (p.fp8)  // the 8-bit tile, widened later
+          tma_load_4d(dst + kStageOff + my_blk * p.bs * D, map, full, 0, 0, c.it.h, phys);
+        else
+          tma_load_4d(dst + my_blk * p.bs * 128 + my_half * kHalfBytes, map, full, 64 * my_half, 0, c.it.h, phys);
+      }
+      ++n;
+      if (++rslot == nslots) {
+        rslot = 0;
+        rphase ^= 1;
+      }
+      cur_next(c);
+      pre = tile_id(c);
+    }
+    if (!ok) fail();
+    // every load issued lands before the CTA can exit
+    for (int u = max(0, n - nslots); u < n; ++u) mbar_wait(bar(full_bar + u % nslots), (u / nslots) & 1);
+    if (is_k)
+      for (int u = max(0, nq - p.nqb); u < nq; ++u) mbar_wait(bar(kBarQFull + q_buf(u)), q_par(u));
+  } else if (warp == kSWarp) {
+    // ======================== Q.K^T issuer (one thread) ========================
+    if (lane == 0) {
       constexpr int KS = D / 16;  // k-steps of Q.K^T
       const uint32_t id_qk = tc_idesc_f16(p.bf16 != 0, false, kTcRows, kTcTok);
-      const uint32_t id_pv = tc_idesc_f16(p.bf16 != 0, true, kTcRows, D);
-      const int ready_bar = p.fp8 ? kBarSlotConv : kBarSlotFull;  // the slot holds 16-bit tiles
+      const int k_ready = p.fp8 ? kBarKConv : kBarKFull;  // the slot holds a 16-bit tile
       const int q_bar = p.q_scale_rows ? kBarQConv : kBarQFull;
-      int rslot = 0, rphase = 0;  // ring step: slot and phase parity
-      auto ring_next = [&]() {
-        if (++rslot == p.nslot) {
-          rslot = 0;
-          rphase ^= 1;
-        }
-      };
-      bool ok = true, issued = false;
-      Cursor sc, pc;  // the tiles whose scores (sc) and P.V (pc) come next
-      cur_start(sc);
-      pc = sc;
-      int sg = 0;  // score tiles issued
-      // S(sg) = Q K^T from `kaddr` into score buffer sg & 1 (after its item's q tile)
-      auto s_issue = [&](uint32_t kaddr) -> bool {
-        if (sc.t == 0 && !mbar_wait(bar(q_bar + (sc.ord & 1)), (sc.ord >> 1) & 1)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t qd = tc_desc_sw128(q_base + (sc.ord & 1) * TB, 16, 1024);
-          const uint64_t kd = tc_desc_sw128(kaddr, 16, 1024);
-          const uint32_t d = tmem + kTmS + 128u * (sg & 1);
-#pragma unroll
-          for (int kk = 0; kk < KS; ++kk) {
-            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-            mma_ss(d, qd + off, kd + off, id_qk, kk > 0);
-          }
-          tc_commit(bar(kBarPh + (sg & 1)));  // phase sg - 2: S(sg) alone
-          if (sc.t == sc.it.ntiles - 1) tc_commit(bar(kBarQEmpty + (sc.ord & 1)));
-        }
-        __syncwarp();
-        ++sg;
-        cur_next(sc);
-        issued = true;
-        return true;
-      };
-      // step 0: S(0) and S(1) alone
-      if (sc.k < nk) {
-        ok = mbar_wait(bar(ready_bar + rslot), rphase) && s_issue(ring_base + rslot * slot_b);
-        if (ok && sc.k < nk) ok = s_issue(ring_base + rslot * slot_b + half_b);
-        if (ok && lane == 0) tc_commit(bar(kBarSlotEmpty + rslot));
-        __syncwarp();
-        ring_next();
-      }
-      int g = 0;  // P.V tiles issued
-      while (ok && pc.k < nk) {
+      int rslot = 0, rphase = 0, j = 0;  // K ring slot and phase parity; score tiles issued
+      bool ok = true;
+      Cursor c;
+      cur_start(c);
+      while (c.k < nk) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        // phase g: P.V(g) with S(g + 2), both tiles in the ring step's slot;
-        // the probabilities, and at an item's first tile the O buffer (read by
-        // the previous item's epilogue).  S(g + 2) reuses the score buffer of
-        // S(g), which its softmax has read before arriving on P(g).
-        const int slot = rslot;
-        if (!(ok = mbar_wait(bar(ready_bar + slot), rphase))) break;
-        const int valid = valid_tokens(pc.it, pc.t);
-        const int nks = (valid + 15) / 16;
-        const uint32_t vb = ring_base + slot * slot_b, kb = vb + half_b;
-        if (valid < nks * 16 && !p.fp8) {
-          // rows past the context in the last k-step hold pool bytes past the
-          // context or stale tiles: zero them so that 0 * junk cannot make NaN
-          // (the E4M3 converter zeroes them itself)
-          const int rows = nks * 16 - valid;
-          for (int w = lane; w < rows * 8 * HALVES; w += 32) {
-            const int row = valid + w / (8 * HALVES), rest = w % (8 * HALVES);
-            st_shared_v4(vb + (rest / 8) * kHalfBytes + row * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (!(ok = mbar_wait(bar(kBarPFull + (g & 1)), (g >> 1) & 1))) break;
-        if (pc.t == 0 && pc.ord >= 1 && !(ok = mbar_wait(bar(kBarOFree), (pc.ord - 1) & 1))) break;
-        const bool with_s = sc.k < nk;
-        if (with_s && sc.t == 0 && !(ok = mbar_wait(bar(q_bar + (sc.ord & 1)), (sc.ord >> 1) & 1))) break;
+        // S(j) into score buffer j & 1 once the item's query tile and K(j)
+        // have landed and the softmax has read S(j - 2) out of the buffer
+        const int qb = q_buf(c.ord);
+        if (c.t == 0 && !(ok = mbar_wait(bar(q_bar + qb), q_par(c.ord)))) break;
+        if (!(ok = mbar_wait(bar(k_ready + rslot), rphase))) break;
+        if (j >= 2 && !(ok = mbar_wait(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1))) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t dO = tmem + kTmO, aP = tmem + kTmP + 64u * (g & 1);
-          const uint64_t vd = tc_desc_sw128(vb, kHalfBytes, 1024);
-          const uint32_t acc0 = pc.t > 0 ? 1u : 0u;
-          if (with_s) {
-            const uint64_t qd = tc_desc_sw128(q_base + (sc.ord & 1) * TB, 16, 1024);
-            const uint64_t kd = tc_desc_sw128(kb, 16, 1024);
-            const uint32_t dS = tmem + kTmS + 128u * (sg & 1);
+        const uint64_t qd = tc_desc_sw128(q_base + qb * TB, 16, 1024);
+        const uint64_t kd = tc_desc_sw128(kring + rslot * slot_b, 16, 1024);
+        const uint32_t dS = tmem + kTmS + 128u * (j & 1);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              if (kk < nks) mma_ts(dO, aP + 8 * kk, vd + ((kk * 2048) >> 4), id_pv, kk > 0 ? 1u : acc0);
-              if (kk < KS) {
-                const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-                mma_ss(dS, qd + off, kd + off, id_qk, kk > 0);
-              }
-            }
-            if (sc.t == sc.it.ntiles - 1) tc_commit(bar(kBarQEmpty + (sc.ord & 1)));
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              if (kk < nks) mma_ts(dO, aP + 8 * kk, vd + ((kk * 2048) >> 4), id_pv, kk > 0 ? 1u : acc0);
-          }
-          tc_commit(bar(kBarPh + (g & 1)));  // phase g: S(g + 2) ready, P buffer g & 1 free
-          tc_commit(bar(kBarSlotEmpty + slot));
-          if (pc.t == pc.it.ntiles - 1) tc_commit(bar(kBarOFull));
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(dS, qd + off, kd + off, id_qk, kk > 0);
         }
-        __syncwarp();
-        ++g;
-        cur_next(pc);
-        if (with_s) {
-          ++sg;
-          cur_next(sc);
+        tc_commit(bar(kBarSFull + (j & 1)));
+        tc_commit(bar(kBarKEmpty + rslot));
+        if (c.t == c.it.ntiles - 1) tc_commit(bar(kBarQEmpty + qb));
+        ++j;
+        if (++rslot == Ly.nks) {
+          rslot = 0;
+          rphase ^= 1;
         }
-        ring_next();
+        cur_next(c);
       }
       if (!ok) fail();
       // every MMA issued has completed before tensor memory is released
-      if (issued) {
-        if (lane == 0) tc_commit(bar(kBarDrain));
-        __syncwarp();
+      if (j > 0) {
+        tc_commit(bar(kBarDrain));
         mbar_wait(bar(kBarDrain), 0);
       }
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ========================== P.V issuer (one warp) ==========================
+    const uint32_t id_pv = tc_idesc_f16(p.bf16 != 0, true, kTcRows, D);
+    const int v_ready = p.fp8 ? kBarVConv : kBarVFull;
+    int rslot = 0, rphase = 0, j = 0;  // V ring slot and phase parity; P.V tiles issued
+    bool ok = true;
+    Cursor c;
+    cur_start(c);
+    while (c.k < nk) {
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      // O += P(j) V(j) once V(j) has landed, the softmax has written P(j), and
+      // at an item's first tile the epilogue has read the previous item's O
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(v_ready + rslot), rphase)))) break;
+      const int valid = valid_tokens(c.it, c.t);
+      const int nks = (valid + 15) / 16;
+      const uint32_t vb = vring + rslot * slot_b;
+      if (valid < nks * 16 && !p.fp8) {
+        // rows past the context in the last k-step hold pool bytes past the
+        // context or stale tiles: zero them so that 0 * junk cannot make NaN
+        // (the E4M3 converter zeroes them itself)
+        const int rows = nks * 16 - valid;
+        for (int w = lane; w < rows * 8 * HALVES; w += 32) {
+          const int row = valid + w / (8 * HALVES), rest = w % (8 * HALVES);
+          st_shared_v4(vb + (rest / 8) * kHalfBytes + row * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPFull + (j & 1)), (j >> 1) & 1)))) break;
+      if (c.t == 0 && c.ord >= 1 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFree), (c.ord - 1) & 1))))
+        break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t dO = tmem + kTmO, aP = tmem + kTmP + 64u * (j & 1);
+        const uint64_t vd = tc_desc_sw128(vb, kHalfBytes, 1024);
+        const uint32_t acc0 = c.t > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (kk < nks) mma_ts(dO, aP + 8 * kk, vd + ((kk * 2048) >> 4), id_pv, kk > 0 ? 1u : acc0);
+        tc_commit(bar(kBarPvDone + (j & 1)));
+        tc_commit(bar(kBarVEmpty + rslot));
+        if (c.t == c.it.ntiles - 1) tc_commit(bar(kBarOFull));
+      }
+      __syncwarp();
+      ++j;
+      if (++rslot == Ly.nvs) {
+        rslot = 0;
+        rphase ^= 1;
+      }
+      cur_next(c);
+    }
+    if (!ok) fail();
+    if (j > 0) {
+      if (lane == 0) tc_commit(bar(kBarDrain + 1));
+      __syncwarp();
+      mbar_wait(bar(kBarDrain + 1), 0);
     }
   } else if (warp < 8) {
     // ============ softmax: one thread per (row, half of the columns) ============
@@ -710,12 +646,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int pos = live ? it.L - p.C + it.j0 + r / p.G : -1;
       const int last = min(pos, it.kv_hi - 1);  // last token this row attends to
       float sl2 = p.scale_log2;                 // this row's score multiplier (base 2)
-      const int qb = ord & 1;
+      const int qb = q_buf(ord);
       if (p.q_scale_rows) {
         // the converter rounded this row of q to f16 after scaling it by 2^e:
-        // 2^-e goes into the row's score multiplier
-        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQConv + qb), (ord >> 1) & 1)))) break;
+        // 2^-e goes into the row's score multiplier; the q buffer (and its
+        // scales) may take another item once every row has read its scale
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQConv + qb), q_par(ord))))) break;
         sl2 *= qsc[qb * kTcRows + r];
+        mbar_arrive(bar(kBarQEmpty + qb));
       }
       float m = -CUDART_INF_F, l = 0.f;  // reference max (base 2) and this half's row sum
       for (int t = 0; t < it.ntiles; ++t, ++g) {
@@ -724,13 +662,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         const int b = g & 1, ph = (g >> 1) & 1;
-        // S(g) is ready, and P buffer b free, once phase g - 2 is done
-        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPh + b), ph)))) break;
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarSFull + b), ph)))) break;
         tc_fence_after();
         float sv[64];
         tmem_ld32(tS + 128u * b, *reinterpret_cast<float(*)[32]>(sv));
         tmem_ld32(tS + 128u * b + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
         tmem_wait_ld();
+        // the score buffer may take S(g + 2)
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree + b));
         const int lim = last - (it.kv_lo + t * kTcTok + 64 * hh);  // last visible column of this half
         if (!__all_sync(0xFFFFFFFFu, lim >= 63)) {
 #pragma unroll
@@ -747,6 +687,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                      fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         mbar_arrive(bar(kBarXchg + b));
         if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarXchg + b), ph)))) break;
+        // P buffer b is free once P.V(g - 2) has completed
+        if (g >= 2 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPvDone + b), ((g - 2) >> 1) & 1)))) break;
         const float mx = sl2 * fmaxf(xs[r], xs[kTcRows + r]);
         const bool bump = mx > m + kRescaleThreshold;  // false while both are -inf
         float alpha = 1.f;
@@ -775,7 +717,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (t > 0 && __any_sync(0xFFFFFFFFu, bump)) {
           // rows whose reference moved rescale their half of the O row once
           // P.V(g - 1) has landed (the others multiply by 1)
-          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPh + (b ^ 1)), ((g + 1) >> 1) & 1)))) break;
+          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPvDone + (b ^ 1)), ((g - 1) >> 1) & 1)))) break;
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
@@ -786,6 +728,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] *= alpha;
             tmem_st32(tO + 32 * c, o);
           }
+        } else {
+          tc_fence_after();
         }
         tmem_st32(tP + 64u * b, pw);
         tmem_wait_st();
@@ -891,8 +835,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // 2^-e goes to the softmax through qsc.  Done before the item's first K
       // tile, in the producer's order, so it never waits on the softmax.
       auto convert_q = [&](const Cursor& c) -> bool {
-        const int qb = c.ord & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQFull + qb), (c.ord >> 1) & 1))) return false;
+        const int qb = q_buf(c.ord);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarQFull + qb), q_par(c.ord)))) return false;
         float mul_inv = 1.f;
         if (r < c.it.ntok * p.G) {
           const uint32_t qrow = q_base + qb * TB + r * 128;
@@ -930,8 +874,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive(bar(kBarQConv + qb));
         return true;
       };
-      int rslot = 0, rphase = 0;  // ring step: slot and phase parity
-      // one tile of a landed slot, widened in place (its half at s16)
+      // one landed tile, widened in place (its 16-bit tile at s16)
       auto convert = [&](const Cursor& c, uint32_t s16) {
         const int valid = valid_tokens(c.it, c.t);
         const uint32_t s8 = s16 + kStageOff;
@@ -972,38 +915,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       };
-      // ring steps as the producer issues them: step 0 = K(0), K(1); step
-      // e >= 1 = V(e - 1), K(e + 1)
+      // the tiles in the order K(0), K(1), then V(j), K(j + 2) for j = 0, 1,
+      // ...; an item's outputs once its last V tile is widened
       Cursor kc, vc;
       cur_start(kc);
       vc = kc;
-      int ke = 0;  // first item whose outputs are not yet written
-      auto step = [&](bool first) -> bool {
-        const int slot = rslot;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarSlotFull + slot), rphase))) return false;
-        const uint32_t dst = ring_base + slot * slot_b;
-        if (first) {
-          if (kc.t == 0 && p.q_scale_rows && !convert_q(kc)) return false;
-          convert(kc, dst);
-          cur_next(kc);
-        } else {
-          convert(vc, dst);
-          cur_next(vc);
-        }
-        if (kc.k < nk) {
-          if (kc.t == 0 && p.q_scale_rows && !convert_q(kc)) return false;
-          convert(kc, dst + half_b);
-          cur_next(kc);
-        }
+      int ks = 0, kph = 0, vs = 0, vph = 0;  // K and V ring slots and phase parities
+      int ke = 0;                            // first item whose outputs are not yet written
+      auto conv_k = [&]() -> bool {
+        if (kc.t == 0 && p.q_scale_rows && !convert_q(kc)) return false;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarKFull + ks), kph))) return false;
+        convert(kc, kring + ks * slot_b);
         fence_proxy_async_smem();
-        mbar_arrive(bar(kBarSlotConv + slot));
-        if (++rslot == p.nslot) {
-          rslot = 0;
-          rphase ^= 1;
+        mbar_arrive(bar(kBarKConv + ks));
+        if (++ks == Ly.nks) {
+          ks = 0;
+          kph ^= 1;
         }
+        cur_next(kc);
         return true;
       };
-      if (kc.k < nk) ok = step(true);
+      auto conv_v = [&]() -> bool {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarVFull + vs), vph))) return false;
+        convert(vc, vring + vs * slot_b);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarVConv + vs));
+        if (++vs == Ly.nvs) {
+          vs = 0;
+          vph ^= 1;
+        }
+        cur_next(vc);
+        return true;
+      };
+      for (int i = 0; ok && i < 2 && kc.k < nk; ++i) ok = conv_k();
       while (ok && vc.k < nk) {
         if (*abort_flag) {
           ok = false;
@@ -1011,7 +955,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const int vk = vc.k;
         const bool item_done = vc.t == vc.it.ntiles - 1;
-        ok = step(false);
+        ok = conv_v();
+        if (ok && kc.k < nk) ok = conv_k();
         if (item_done)
           for (; ok && ke <= vk; ++ke) ok = epilogue(ke);
       }
@@ -1022,7 +967,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1041,18 +986,19 @@ cudaError_t launch_d(const TcParams& p, const CUtensorMap& tmQ, const CUtensorMa
 
 }  // namespace
 
-int tc_ring_slots(int D, int fp8) {
-  const Layout L0 = layout_of(D, 0, fp8);
+int tc_ring_slots(int D, int fp8, int nqb) {
+  const Layout L0 = layout_of(D, 0, fp8, nqb);
   const int n = (kSmemLimit - L0.total) / L0.slot;
   return n < kTcMaxSlots ? n : kTcMaxSlots;
 }
 
-int tc_smem_bytes(int D, int nslot, int fp8) { return layout_of(D, nslot, fp8).total; }
+int tc_smem_bytes(int D, int nslot, int fp8, int nqb) { return layout_of(D, nslot, fp8, nqb).total; }
 
 cudaError_t launch_attn_tc(const TcParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            cudaStream_t st) {
-  if (p.nslot < 2 || p.nslot > kTcMaxSlots || (p.D != 64 && p.D != 128)) return cudaErrorInvalidValue;
-  const int smem = tc_smem_bytes(p.D, p.nslot, p.fp8);
+  if (p.nslot < 2 || p.nslot > kTcMaxSlots || (p.D != 64 && p.D != 128) || (p.nqb != 1 && p.nqb != 2))
+    return cudaErrorInvalidValue;
+  const int smem = tc_smem_bytes(p.D, p.nslot, p.fp8, p.nqb);
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
   static std::atomic<int> sms[64];
   int dev = 0;

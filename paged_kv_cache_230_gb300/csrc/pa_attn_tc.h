@@ -36,6 +36,7 @@ struct TcParams {
   int Pmax;            // split: partitions per sequence at most
   int ppc;             // split: partitions per run
   int nslot;           // K/V ring slots
+  int nqb;             // query tile buffers in shared memory (1 or 2)
   int rank_seqs;       // 1: items ordered by context length, longest first
   int bf16;            // MMA operands (q, K, V, P): 1 bf16, 0 f16
   int out_bf16;        // output (and q) dtype: 1 bf16, 0 f16
@@ -46,10 +47,10 @@ struct TcParams {
   float vscale;        // kv_scale for FP8 caches, 1 otherwise
 };
 
-// Ring slots and dynamic shared memory for a launch with head_dim D and
-// 16-bit (fp8 = 0) or E4M3 (fp8 = 1) caches.
-int tc_ring_slots(int D, int fp8);
-int tc_smem_bytes(int D, int nslot, int fp8);
+// Ring slots and dynamic shared memory for a launch with head_dim D,
+// 16-bit (fp8 = 0) or E4M3 (fp8 = 1) caches and nqb query tile buffers.
+int tc_ring_slots(int D, int fp8, int nqb);
+int tc_smem_bytes(int D, int nslot, int fp8, int nqb);
 
 // tmQ: 3-D map over q {D, Hq, S * C}, box {64, G, T}, 128-byte swizzle;
 // tmK / tmV: the caches' 4-D maps (16-bit: box {64, bs, 1, 1}, 128-byte

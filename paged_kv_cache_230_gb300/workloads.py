@@ -393,13 +393,14 @@ def make_config(idx: int, seed: Optional[int] = None, fill_unused: str = "normal
 
 
 def make_prefill_workload(S: int = 16, C: int = 2048, bs: int = 16, seed: int = 7,
-                          fill_unused: str = "normal") -> Workload:
+                          fill_unused: str = "normal", kv_dtype: str = BF16, D: int = 128) -> Workload:
     """The chunked-prefill batch: S sequences, each with a chunk of C new
     tokens at the end of a context of 2C (so every query attends to between
-    C + 1 and 2C tokens), GQA-8B heads (32 query / 8 kv heads), head_dim 128,
-    bf16, block size bs."""
-    return make_workload(name="prefill_gqa8b", seed=seed, context_lens=[2 * C] * S, Hq=32, Hkv=8, D=128, bs=bs,
-                         q_dtype=BF16, kv_dtype=BF16, qlen=C, fill_unused=fill_unused)
+    C + 1 and 2C tokens), GQA-8B heads (32 query / 8 kv heads), head_dim D
+    (128 by default), bf16 q, bf16 or E4M3 caches, block size bs."""
+    name = "prefill_gqa8b" + ("_fp8" if kv_dtype == FP8 else "") + ("" if D == 128 else "_d%d" % D)
+    return make_workload(name=name, seed=seed, context_lens=[2 * C] * S, Hq=32, Hkv=8, D=D, bs=bs,
+                         q_dtype=BF16, kv_dtype=kv_dtype, qlen=C, fill_unused=fill_unused)
 
 
 def subset(wl: Workload, seqs) -> Workload:
