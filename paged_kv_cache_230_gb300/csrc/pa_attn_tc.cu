@@ -224,6 +224,15 @@ __device__ Item item_of(const TcParams& p, const int* seq_tab, const int* len_ta
   const int per_seq = p.Hkv * per_h;
   const int rank = idx / per_seq;
   int rem = idx - rank * per_seq;
+  // split: the items of one sequence are rotated by rank * delta (delta about
+  // 0.38 R), so that a CTA whose index keeps landing on the same run (the grid
+  // a multiple of the items per sequence) meets runs spread over the whole
+  // range instead of always the first (which every context has) or always
+  // the last (which few have)
+  if (p.R > 1) {
+    const int64_t delta = max(1, (p.R * 5 + 6) / 13);
+    rem = static_cast<int>((rem + (static_cast<int64_t>(rank) * delta) % per_seq) % per_seq);
+  }
   it.h = rem / per_h;
   rem -= it.h * per_h;
   it.qt = p.n_qt - 1 - rem / p.R;

@@ -248,3 +248,59 @@ def test_scale_must_be_positive_on_the_tensor_core_path():
         with pytest.raises(pa.PagedAttnError) as e:
             pa.decode_multi(q.clone(), q, kc, kc, bt, cl, bad)
         assert e.value.status == -1
+
+
+@pytest.mark.parametrize("P", [0, 512])
+def test_graph_captured_launch_replays_the_oracle_result(P):
+    """The tensor-core path captured into a CUDA graph (tensor maps and
+    parameters baked into the graph, the split workspace allocated before
+    capture): replays give the eager launch's bits, within the oracle's
+    tolerance, and agree with each other."""
+    wl = W.make_workload(name="t", seed=66, context_lens=LENS + [3000, 4097], Hq=32, Hkv=8, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=8)
+    pa = _gpu.lib()
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    eager = g.decode(partition_size=P).clone()
+    torch.cuda.synchronize()
+    kc, vc = _gpu.oracle_pool(wl)
+    want = _gpu.oracle_out(wl, kc, vc, partition_size=P)
+    assert _gpu.max_err(eager, want) <= _gpu.tolerance(wl)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        g.decode(partition_size=P)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.decode(partition_size=P)
+    for _ in range(2):
+        g.out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 0
+        assert torch.equal(g.out, eager)
+    _check_zero_rows(g.out, wl)
+
+
+def test_concurrent_launches_on_many_streams_agree():
+    """Launches on 80 streams at once (the kernel keeps no state between
+    launches) all give the single-stream result bit for bit."""
+    wl = W.make_workload(name="t", seed=67, context_lens=[700, 33, 1500], Hq=32, Hkv=8, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=8)
+    pa = _gpu.lib()
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    ref = g.decode().clone()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(80)]
+    outs = [torch.empty_like(g.q) for _ in streams]
+    for s, o in zip(streams, outs):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            pa.decode_multi(o, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    for o in outs:
+        assert torch.equal(o, ref)
