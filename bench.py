@@ -57,8 +57,9 @@ def parse():
     ap.add_argument("--block-size", type=int, default=16, help="KV block size of the prefill workload (8, 16, 32)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache dtype of the prefill workload")
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128], help="head_dim of the prefill workload")
-    ap.add_argument("--op", default="decode", choices=["decode", "blocks", "prefill"],
-                    help="blocks: time copy-on-write block copies and swap-out/in through pinned host memory")
+    ap.add_argument("--op", default="decode", choices=["decode", "blocks", "prefill", "l2read"],
+                    help="blocks: time copy-on-write block copies and swap-out/in through pinned host memory; "
+                         "l2read: measure the rate at which the SMs read an L2-resident buffer")
     ap.add_argument("--ref-budget", type=float, default=0.0,
                     help="reference arm: seconds of oracle work per step (default min(20, 120 / steps))")
     return ap.parse_args()
@@ -529,6 +530,53 @@ def e2e_measure(b, wl, dev, K, warm, pg):
             "pipelining": "two buffer sets; copies on a second stream overlap other steps' kernels"}
 
 
+def run_l2read(args, local):
+    """The L2 -> SM read rate: a 64 MiB buffer (half of L2) read once, then
+    timed over launches of pa_probe_l2_read with plain 16-byte loads (mode 0)
+    and with the 2 KB TMA boxes the attention kernels load K/V with (mode 1).
+    Median and best of 7 launches of about 12 GB each; no setting changed."""
+    import torch
+    from paged_kv_cache_230_gb300 import build as _build
+    _build.build()
+    from paged_kv_cache_230_gb300 import pagedattn as pa
+    torch.cuda.set_device(local)
+    nbytes = 64 << 20
+    buf = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    nsm = torch.cuda.get_device_properties(local).multi_processor_count
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+        sampler.mark(True)
+    res = {}
+    for mode, iters in ((0, 192), (1, max(1, int(12e9 / (nsm * 32768))))):
+        for _ in range(2):
+            pa.probe_l2_read(buf, mode, iters, sink)
+        torch.cuda.synchronize()
+        rates = []
+        for _ in range(7):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            nread = pa.probe_l2_read(buf, mode, iters, sink)
+            e1.record()
+            torch.cuda.synchronize()
+            rates.append(nread / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        res[mode] = (statistics.median(rates), max(rates), nread)
+    if sampler:
+        sampler.mark(False)
+    clocks = sampler.stop() if sampler else None
+    assert pa.get_device_error() == 0
+    line = {"metric": "L2 -> SM read bandwidth", "value": res[0][0], "unit": "GB/s", "n_gpus": 1, "steps": 7,
+            "higher_is_better": True, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": "l2_resident_buffer", "buffer_bytes": nbytes, "bytes_per_launch_plain": res[0][2],
+                       "bytes_per_launch_tma": res[1][2]},
+            "plain_loads_gbs": {"median": res[0][0], "best": res[0][1]},
+            "tma_boxes_gbs": {"median": res[1][0], "best": res[1][1]},
+            "clocks": clocks, "gpu_launches": 14}
+    print(json.dumps(line), flush=True)
+
+
 def run_blocks(args, local):
     """Whole-block moves on the gqa8b pool shape (8 kv heads x 16 tokens x 128
     channels, bf16: 32 KiB per block per cache): pa_copy_blocks of 4096
@@ -682,9 +730,9 @@ def run_prefill(args, local):
 def main():
     args = parse()
     world, rank, local, pg = dist_setup()
-    if args.op in ("blocks", "prefill"):
+    if args.op in ("blocks", "prefill", "l2read"):
         if rank == 0:
-            (run_blocks if args.op == "blocks" else run_prefill)(args, local)
+            {"blocks": run_blocks, "prefill": run_prefill, "l2read": run_l2read}[args.op](args, local)
         return
     if args.impl == "reference" and rank != 0:
         return

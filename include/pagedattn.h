@@ -384,6 +384,26 @@ PA_API int pa_get_device_error(void);
  */
 PA_API int pa_selftest_wait_timeout(pa_stream_t stream);
 
+/*
+ * pa_probe_l2_read: measurement utility, not part of the attention path.
+ * Enqueues on `stream` one kernel that reads the device buffer `buf` (16-byte
+ * aligned, `bytes` long; make it smaller than L2 and read it once beforehand
+ * so that it sits in L2) and writes nothing but, when a checksum of the data
+ * equals a fixed pattern, 4 bytes at `sink` (device memory): timing the
+ * launch with events gives the rate at which the SMs read from L2, the bound
+ * of a decode whose K/V blocks are shared by many sequences.
+ *   mode 0: `iters` passes over the whole buffer with plain 16-byte loads
+ *           cached in L2 only (bytes a multiple of 16);
+ *   mode 1: TMA boxes of 16 rows x 128 bytes, the box the attention kernels
+ *           load K/V tiles with: one CTA per SM issues `iters` stages of 16
+ *           boxes each (bytes a multiple of 2048).
+ * *bytes_read (host memory) receives the bytes the launch reads.  Returns
+ * PA_OK, PA_ERR_INVALID_ARG for a null pointer, a misaligned buffer, a size
+ * the mode cannot use or iters <= 0, or PA_ERR_CUDA if the launch fails.
+ */
+PA_API int pa_probe_l2_read(const void* buf, size_t bytes, int32_t mode, int32_t iters, void* sink,
+                            unsigned long long* bytes_read, pa_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 PA_API int pa_version(void);
 

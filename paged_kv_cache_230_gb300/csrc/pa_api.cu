@@ -434,6 +434,9 @@ int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
 namespace pa {
 // pa_selftest.cu: one kernel whose bounded wait runs out
 cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t st);
+cudaError_t launch_l2_read_plain(const void* buf, size_t bytes, int iters, void* sink, int nsm, cudaStream_t st);
+cudaError_t launch_l2_read_tma(const CUtensorMap& map, int nrows, int iters, void* sink, int* err, int nsm,
+                               cudaStream_t st);
 }  // namespace pa
 
 extern "C" {
@@ -743,6 +746,38 @@ int pa_selftest_wait_timeout(pa_stream_t stream) {
   if (!err) return PA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return pa::launch_wait_timeout_selftest(err, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_probe_l2_read(const void* buf, size_t bytes, int32_t mode, int32_t iters, void* sink,
+                     unsigned long long* bytes_read, pa_stream_t stream) {
+  if (!buf || !sink || !bytes_read || iters <= 0 || !aligned16(buf) || (mode != 0 && mode != 1))
+    return PA_ERR_INVALID_ARG;
+  if (mode == 0 && (bytes < 16 || bytes % 16)) return PA_ERR_INVALID_ARG;
+  if (mode == 1 && (bytes < 2048 || bytes % 2048 || bytes / 128 > INT32_MAX)) return PA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  const int nsm = sm_count();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == 0) {
+    *bytes_read = static_cast<unsigned long long>(bytes) * static_cast<unsigned long long>(iters);
+    return pa::launch_l2_read_plain(buf, bytes, iters, sink, nsm, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  // rows of 128 bytes, boxes of 16 rows with the 128-byte swizzle
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {64, cuuint64_t(bytes / 128)};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(buf), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_CUDA;
+  *bytes_read = static_cast<unsigned long long>(nsm) * static_cast<unsigned long long>(iters) * 32768ull;
+  return pa::launch_l2_read_tma(map, static_cast<int>(bytes / 128), iters, sink, err, nsm, st) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 int pa_version(void) { return 100; }

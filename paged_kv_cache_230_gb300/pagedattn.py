@@ -36,7 +36,7 @@ EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
            "pa_bm_free_sequence", "pa_bm_block_table", "pa_bm_num_free_blocks", "pa_bm_refcount",
            "pa_bm_tail_waste", "pa_bm_check", "pa_status_string", "pa_set_check_mode", "pa_get_device_error",
-           "pa_selftest_wait_timeout", "pa_version"]
+           "pa_selftest_wait_timeout", "pa_probe_l2_read", "pa_version"]
 
 
 class PagedAttnError(RuntimeError):
@@ -103,12 +103,14 @@ def _load() -> ctypes.CDLL:
     lib.pa_set_check_mode.argtypes = [ctypes.c_int]
     lib.pa_get_device_error.argtypes = []
     lib.pa_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+    lib.pa_probe_l2_read.argtypes = [P, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32, P,
+                                     ctypes.POINTER(ctypes.c_ulonglong), P]
     lib.pa_version.argtypes = []
     for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_decode_split", "pa_decode_multi_split",
                  "pa_cache_and_decode",
                  "pa_decode_split_noalloc",
                  "pa_set_check_mode",
-                 "pa_get_device_error", "pa_selftest_wait_timeout", "pa_version"):
+                 "pa_get_device_error", "pa_selftest_wait_timeout", "pa_probe_l2_read", "pa_version"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -372,6 +374,20 @@ def selftest_wait_timeout() -> None:
     DEVERR_TIMEOUT in the device error word and returns (read it with
     get_device_error())."""
     _check("pa_selftest_wait_timeout", lib.pa_selftest_wait_timeout(_stream(torch.device("cuda", torch.cuda.current_device()))))
+
+
+def probe_l2_read(buf: torch.Tensor, mode: int, iters: int, sink: torch.Tensor) -> int:
+    """Enqueue, on torch's current stream, the L2 read-rate probe over the
+    bytes of `buf` (a contiguous CUDA tensor; mode 0: plain 16-byte loads,
+    `iters` passes over the buffer; mode 1: TMA boxes of 16 x 128 bytes,
+    `iters` 32 KB stages per SM).  `sink` is a CUDA tensor of at least 4 bytes.
+    Returns the bytes the launch reads."""
+    if not buf.is_cuda or not buf.is_contiguous() or not sink.is_cuda or sink.numel() * sink.element_size() < 4:
+        raise ValueError("probe_l2_read wants a contiguous CUDA buffer and a CUDA sink of at least 4 bytes")
+    n = ctypes.c_ulonglong(0)
+    _check("pa_probe_l2_read", lib.pa_probe_l2_read(_ptr(buf), buf.numel() * buf.element_size(), int(mode),
+                                                      int(iters), _ptr(sink), ctypes.byref(n), _stream(buf.device)))
+    return int(n.value)
 
 
 def get_device_error() -> int:
