@@ -268,12 +268,20 @@ struct Cursor {
   Item it;
 };
 
-template <int D>
+// KIND: 0 f16 q and caches, 1 bf16 q and caches, 2 f16 q with E4M3 caches,
+// 3 bf16 q with E4M3 caches (an instantiation per kind keeps each one's
+// code to its own path: the warps of six roles share an SM's instruction
+// caches).
+template <int D, int KIND>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
   constexpr int TB = tile_bytes(D);
   constexpr int HALVES = D / 64;
+  constexpr bool kFp8 = KIND >= 2;                         // E4M3 caches, widened to f16
+  constexpr bool kBf16 = KIND == 1;                        // MMA operands and P in bf16 (else f16)
+  constexpr bool kOutBf16 = KIND == 1 || KIND == 3;        // q and output dtype
+  constexpr bool kQScale = KIND == 3;                      // bf16 q rounded to f16 per row
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = smem_u32(smem);
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) atomicOr(p.err, kErrLayout);
     return;
   }
-  const Layout Ly = layout_of(D, p.nslot, p.fp8, p.nqb);
+  const Layout Ly = layout_of(D, p.nslot, kFp8, p.nqb);
   const uint32_t bar0 = base + Ly.tail;
   auto bar = [&](int k) -> uint32_t { return bar0 + 8u * k; };
   uint8_t* tail = smem + Ly.tail;
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarQFull + i), 1);
-      mbar_init(bar(kBarQEmpty + i), p.q_scale_rows ? 1 + 2 * kTcRows : 1);
+      mbar_init(bar(kBarQEmpty + i), kQScale ? 1 + 2 * kTcRows : 1);
       mbar_init(bar(kBarQConv + i), kTcRows);
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSFree + i), 2 * kTcRows);
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // 128 / 8 blocks x 2 halves = 32 boxes.
     const bool is_k = warp == kKProdWarp;
     const CUtensorMap* map = is_k ? &tmK : &tmV;
-    const int bpb = p.fp8 ? 1 : HALVES;  // boxes per block
+    const int bpb = kFp8 ? 1 : HALVES;  // boxes per block
     const int my_blk = lane / bpb, my_half = lane % bpb;
     const int nslots = is_k ? Ly.nks : Ly.nvs;
     const uint32_t ring = is_k ? kring : vring;
@@ -505,13 +513,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t full = bar(full_bar + rslot), dst = ring + rslot * slot_b;
       int b0;
       const int nb = tile_blocks(c, b0);
-      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * p.bs * D * (p.fp8 ? 1 : 2)));
+      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * p.bs * D * (kFp8 ? 1 : 2)));
       __syncwarp();
       if (my_blk < nb) {
         const int phys = pre;
         if (is_k && my_half == 0 && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks))
           atomicOr(p.err, kErrBlockId);
-        if (p.fp8)  // the 8-bit tile, widened later
+        if (kFp8)  // the 8-bit tile, widened later
           tma_load_4d(dst + kStageOff + my_blk * p.bs * D, map, full, 0, 0, c.it.h, phys);
         else
           tma_load_4d(dst + my_blk * p.bs * 128 + my_half * kHalfBytes, map, full, 64 * my_half, 0, c.it.h, phys);
@@ -533,9 +541,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ======================== Q.K^T issuer (one thread) ========================
     if (lane == 0) {
       constexpr int KS = D / 16;  // k-steps of Q.K^T
-      const uint32_t id_qk = tc_idesc_f16(p.bf16 != 0, false, kTcRows, kTcTok);
-      const int k_ready = p.fp8 ? kBarKConv : kBarKFull;  // the slot holds a 16-bit tile
-      const int q_bar = p.q_scale_rows ? kBarQConv : kBarQFull;
+      const uint32_t id_qk = tc_idesc_f16(kBf16, false, kTcRows, kTcTok);
+      const int k_ready = kFp8 ? kBarKConv : kBarKFull;  // the slot holds a 16-bit tile
+      const int q_bar = kQScale ? kBarQConv : kBarQFull;
       int rslot = 0, rphase = 0, j = 0;  // K ring slot and phase parity; score tiles issued
       bool ok = true;
       Cursor c;
@@ -580,8 +588,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp == kPvWarp) {
     // ========================== P.V issuer (one warp) ==========================
-    const uint32_t id_pv = tc_idesc_f16(p.bf16 != 0, true, kTcRows, D);
-    const int v_ready = p.fp8 ? kBarVConv : kBarVFull;
+    const uint32_t id_pv = tc_idesc_f16(kBf16, true, kTcRows, D);
+    const int v_ready = kFp8 ? kBarVConv : kBarVFull;
     int rslot = 0, rphase = 0, j = 0;  // V ring slot and phase parity; P.V tiles issued
     bool ok = true;
     Cursor c;
@@ -597,7 +605,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int valid = valid_tokens(c.it, c.t);
       const int nks = (valid + 15) / 16;
       const uint32_t vb = vring + rslot * slot_b;
-      if (valid < nks * 16 && !p.fp8) {
+      if (valid < nks * 16 && !kFp8) {
         // rows past the context in the last k-step hold pool bytes past the
         // context or stale tiles: zero them so that 0 * junk cannot make NaN
         // (the E4M3 converter zeroes them itself)
@@ -656,7 +664,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int last = min(pos, it.kv_hi - 1);  // last token this row attends to
       float sl2 = p.scale_log2;                 // this row's score multiplier (base 2)
       const int qb = q_buf(ord);
-      if (p.q_scale_rows) {
+      if (kQScale) {
         // the converter rounded this row of q to f16 after scaling it by 2^e:
         // 2^-e goes into the row's score multiplier; the q buffer (and its
         // scales) may take another item once every row has read its scale
@@ -722,13 +730,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
         uint32_t pw[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pw[c] = pack16(sv[2 * c], sv[2 * c + 1], p.bf16);
+        for (int c = 0; c < 32; ++c) pw[c] = pack16(sv[2 * c], sv[2 * c + 1], kBf16);
         if (t > 0 && __any_sync(0xFFFFFFFFu, bump)) {
           // rows whose reference moved rescale their half of the O row once
           // P.V(g - 1) has landed (the others multiply by 1)
           if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPvDone + (b ^ 1)), ((g - 1) >> 1) & 1)))) break;
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1  // rare: rolled, so that it takes little of the instruction caches
           for (int c = 0; c < D / 64; ++c) {
             float o[32];
             tmem_ld32(tO + 32 * c, o);
@@ -787,7 +795,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m = m_buf[r];
       }
       const float inv = l > 0.f ? p.vscale / l : 0.f;
-#pragma unroll
+      // a rolled loop: once per item, and its code shares the instruction
+      // caches with the converter's and the softmax's
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         if (have) {
@@ -808,10 +818,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
-            w.x = pack16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv, p.out_bf16);
-            w.y = pack16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv, p.out_bf16);
-            w.z = pack16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv, p.out_bf16);
-            w.w = pack16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv, p.out_bf16);
+            w.x = pack16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv, kOutBf16);
+            w.y = pack16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv, kOutBf16);
+            w.z = pack16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv, kOutBf16);
+            w.w = pack16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv, kOutBf16);
             *reinterpret_cast<uint4*>(orow + q4 * 8) = w;
           }
         } else {
@@ -830,7 +840,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (have) ++ord;
       return true;
     };
-    if (!p.fp8) {
+    if (!kFp8) {
       for (int k = 0; ok && k < nk; ++k) ok = epilogue(k);
     } else {
       // E4M3 caches: every ring load, in the order the producer issues them,
@@ -932,7 +942,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int ks = 0, kph = 0, vs = 0, vph = 0;  // K and V ring slots and phase parities
       int ke = 0;                            // first item whose outputs are not yet written
       auto conv_k = [&]() -> bool {
-        if (kc.t == 0 && p.q_scale_rows && !convert_q(kc)) return false;
+        if (kc.t == 0 && kQScale && !convert_q(kc)) return false;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarKFull + ks), kph))) return false;
         convert(kc, kring + ks * slot_b);
         fence_proxy_async_smem();
@@ -982,11 +992,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int KIND>
 cudaError_t launch_d(const TcParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                      int grid, int smem, cudaStream_t st) {
   // every warp role fits in the 128 registers a thread of the 512 gets
-  auto kern = attn_tc_kernel<D>;
+  auto kern = attn_tc_kernel<D, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kTcThreads, smem, st>>>(tmQ, tmK, tmV, p);
@@ -1024,7 +1034,21 @@ cudaError_t launch_attn_tc(const TcParams& p, const CUtensorMap& tmQ, const CUte
   TcParams q = p;
   // items per CTA beyond the table are not ordered
   if ((p.total + grid - 1) / grid > kTcMaxRanked) q.rank_seqs = 0;
-  return p.D == 64 ? launch_d<64>(q, tmQ, tmK, tmV, grid, smem, st) : launch_d<128>(q, tmQ, tmK, tmV, grid, smem, st);
+  // the kind of the launch: the operand dtype (bf16, or f16 for E4M3 caches),
+  // the q and output dtype, whether bf16 q is rounded to f16 per row
+  if (p.fp8 ? (p.bf16 != 0 || p.q_scale_rows != p.out_bf16) : (p.bf16 != p.out_bf16 || p.q_scale_rows != 0))
+    return cudaErrorInvalidValue;
+  const int kind = p.fp8 ? (p.out_bf16 ? 3 : 2) : (p.bf16 ? 1 : 0);
+  switch (kind + 4 * (p.D == 64 ? 0 : 1)) {
+    case 0: return launch_d<64, 0>(q, tmQ, tmK, tmV, grid, smem, st);
+    case 1: return launch_d<64, 1>(q, tmQ, tmK, tmV, grid, smem, st);
+    case 2: return launch_d<64, 2>(q, tmQ, tmK, tmV, grid, smem, st);
+    case 3: return launch_d<64, 3>(q, tmQ, tmK, tmV, grid, smem, st);
+    case 4: return launch_d<128, 0>(q, tmQ, tmK, tmV, grid, smem, st);
+    case 5: return launch_d<128, 1>(q, tmQ, tmK, tmV, grid, smem, st);
+    case 6: return launch_d<128, 2>(q, tmQ, tmK, tmV, grid, smem, st);
+    default: return launch_d<128, 3>(q, tmQ, tmK, tmV, grid, smem, st);
+  }
 }
 
 }  // namespace pa
