@@ -207,7 +207,7 @@ DECODE_SOURCES = ("pa_decode.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_decode_f16
 TC_SOURCES = ("pa_attn_tc.cu", "pa_attn_tc.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
 
 
-PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill.h") + TC_SOURCES
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
 
 
 def kernel_source_hash(sources=DECODE_SOURCES) -> str:
@@ -246,12 +246,12 @@ def recorded_traffic(workload: str, kernel: str):
         return None
 
 
-def recorded_prefill_traffic(name: str, chunk: int, seqs: int):
+def recorded_prefill_traffic(name: str, chunk: int, seqs: int, sources=PREFILL_SOURCES):
     """DRAM bytes of one prefill launch over `seqs` sequences with a `chunk`-token
     chunk at context 2 x chunk: the captured bytes per sequence (every
     sequence reads its own q, K and V and writes its own output) times seqs."""
     try:
-        per_seq = float(_profile_values("%s_chunk%d" % (name, chunk), PREFILL_SOURCES)["dram_bytes_per_sequence"])
+        per_seq = float(_profile_values("%s_chunk%d" % (name, chunk), sources)["dram_bytes_per_sequence"])
     except (KeyError, ValueError):
         return None
     return per_seq * seqs
@@ -675,6 +675,11 @@ def run_prefill(args, local):
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
     flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())
+    # 16-bit head_dim-128 caches go to the per-head kernel, E4M3 caches and
+    # head_dim 64 to the tensor-core kernel with the GQA heads packed in rows
+    per_head = kv != W.FP8 and wl.D == 128
+    kernel = "pa_prefill (prefill_kernel)" if per_head else "pa_prefill (attn_tc_kernel)"
+    sources = PREFILL_SOURCES if per_head else TC_SOURCES
 
     def run():
         pa.prefill(b.out, b.q, b.k_cache, b.v_cache, b.block_tables, b.context_lens, wl.scale, wl.kv_scale)
@@ -723,7 +728,7 @@ def run_prefill(args, local):
             "prefill_us": us, "tokens_per_s": S * C / (us * 1e-6), "clocks": clocks,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "peak_source": kind, "frac_of_burst_peak": tflops / burst,
-                         "traffic": recorded_prefill_traffic(wl.name, C, S), "kernel": "pa_prefill"}}
+                         "traffic": recorded_prefill_traffic(wl.name, C, S, sources), "kernel": kernel}}
     print(json.dumps(line), flush=True)
 
 
