@@ -284,8 +284,17 @@ def oracle_sample_time(wl: W.Workload, budget_s: float = 20.0, threads: int = 0)
         t0 = time.perf_counter()
         oracle.reshape_and_cache(sub.key, sub.value, sub.q_dtype, kc, vc, sub.kv_dtype, sub.slot_mapping,
                                  sub.kv_scale)
-        oracle.decode(sub.q, sub.q_dtype, kc, vc, sub.kv_dtype, sub.block_tables, sub.context_lens, sub.scale,
-                      sub.kv_scale, partition_size=sub.partition_size, num_threads=threads)
+        if sub.qlen == 1:
+            oracle.decode(sub.q, sub.q_dtype, kc, vc, sub.kv_dtype, sub.block_tables, sub.context_lens, sub.scale,
+                          sub.kv_scale, partition_size=sub.partition_size, num_threads=threads)
+        else:
+            # new token j of k attends causally to the prefix ending at its
+            # position L - k + j: the oracle decodes it as its own query
+            k = sub.qlen
+            L = (sub.context_lens[:, None] - k + 1 + np.arange(k)[None, :]).reshape(-1)
+            oracle.decode(sub.q.reshape(sub.S * k, sub.Hq, sub.D), sub.q_dtype, kc, vc, sub.kv_dtype,
+                          np.repeat(sub.block_tables, k, axis=0), np.maximum(L, 0).astype(np.int32), sub.scale,
+                          sub.kv_scale, partition_size=sub.partition_size, num_threads=threads)
         total_t += time.perf_counter() - t0
         total_b += sub.kv_bytes()
         nseq += len(sel)
