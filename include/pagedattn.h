@@ -154,12 +154,14 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * num_q_tokens new tokens per sequence (positions L - C .. L - 1 of each
  * context; chunked prefill, review §10 table), computed on the tensor cores
  * with tcgen05 MMAs and tensor-memory accumulators: prefill is the
- * compute-bound phase (review §7).  The queries of a (sequence, kv head) are
- * packed as rows token * G + head, floor(128 / G) tokens x G heads per
- * 128-row tile, so every K/V tile loaded serves all G heads; a work item
- * holds two such tiles, whose MMAs alternate on the tensor core.  The kernel
- * is persistent, one CTA per SM walking the items (longest contexts first),
- * and streams each item's 128-token K/V tiles through the block table.
+ * compute-bound phase (review §7).  With E4M3 caches or head_dim 64 the
+ * queries of a (sequence, kv head) are packed as rows token * G + head,
+ * floor(128 / G) tokens x G heads per 128-row tile, so every K/V tile loaded
+ * serves all G heads (the kernel of the wide-group decode calls).  With
+ * 16-bit caches and head_dim 128 a work item is (sequence, query head, 128
+ * new tokens) of a kernel built for that shape, which measured faster there.
+ * Both are persistent, one CTA per SM walking the items (longest contexts
+ * first), and stream each item's 128-token K/V tiles through the block table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
  * Supported: head_dim 64 or 128, caches of the q dtype or FP8 E4M3, block
  * size 8, 16 or 32, G up to 128, scale > 0.  E4M3 tiles are widened exactly
