@@ -204,6 +204,17 @@ __device__ __forceinline__ int length_bucket(int L) {
   return 127 - min(msb * 4 + frac, 127);
 }
 
+// Global index of this CTA's k-th work item.  Round k of the grid covers
+// indices k * grid .. k * grid + grid - 1; CTA c takes the c-th of them, and
+// without split runs the (grid - 1 - c)-th in odd rounds (a snake: the long
+// items at the head of the longest-first list spread evenly over the CTAs).
+// The split form keeps c-th in every round, its runs rotated per sequence
+// instead (item_of).
+__device__ __forceinline__ int item_index(const TcParams& p, int k) {
+  const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * grid + ((p.R == 1 && (k & 1)) ? grid - 1 - c : c);
+}
+
 struct Item {
   int s, h, qt, run, L;
   int j0, ntok;        // first new token of the query tile and how many it holds
@@ -213,13 +224,13 @@ struct Item {
   bool final_out;      // the item writes normalised outputs (not a split partial)
 };
 
-// Work item k of this CTA (global index blockIdx.x + k * gridDim.x).  With
+// Work item k of this CTA (global index item_index(p, k)).  With
 // at most kTcMaxRanked items per CTA their sequences and context lengths
 // come from the tables built at start-up (shared memory, no global load on
 // the pipeline's path).
 __device__ Item item_of(const TcParams& p, const int* seq_tab, const int* len_tab, bool tabs, int k) {
   Item it;
-  const int idx = blockIdx.x + k * gridDim.x;
+  const int idx = item_index(p, k);
   const int per_h = p.n_qt * p.R;
   const int per_seq = p.Hkv * per_h;
   const int rank = idx / per_seq;
@@ -305,8 +316,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* qsc = reinterpret_cast<float*>(tail + kQscOff);    // [2 q buffers][128]
   const uint32_t q_base = base + Ly.q, kring = base + Ly.kring, vring = base + Ly.vring;
   const int slot_b = Ly.slot;
-  const int nk = (p.total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                 static_cast<int>(gridDim.x);  // this CTA's work items
+  // this CTA's work items: every full round, and the last partial one if its
+  // place in that round is below the items left over
+  const int rounds = p.total / static_cast<int>(gridDim.x);
+  const int nk = rounds + (item_index(p, rounds) < p.total ? 1 : 0);
   const bool tabs = nk <= kTcMaxRanked;
   // the q buffer of the item with ordinal o among those with tiles, and the
   // parity of that buffer's phase for it
@@ -373,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     const int per_seq = p.Hkv * p.n_qt * p.R;
     for (int k = warp; k < nk; k += kTcThreads / 32) {
-      const int rank = (static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x)) / per_seq;
+      const int rank = item_index(p, k) / per_seq;
       // the bucket holding rank, then the rank's place among that bucket's
       // sequences in index order
       int mine = -1;
@@ -404,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (tabs) {
     const int per_seq = p.Hkv * p.n_qt * p.R;
-    for (int k = tid; k < nk; k += kTcThreads) seq_tab[k] = (static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x)) / per_seq;
+    for (int k = tid; k < nk; k += kTcThreads) seq_tab[k] = item_index(p, k) / per_seq;
   }
   if (tabs) {
     __syncthreads();
