@@ -1,6 +1,7 @@
 // Log-sum-exp merge of split-decode partials (the second kernel of
 // pa_decode_split and pa_decode_multi_split).
 #include "pa_decode.cuh"
+#include "pa_pdl.cuh"
 
 namespace pa {
 
@@ -37,6 +38,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodePa
   __shared__ float wsh[kMergeMaxParts];
   __shared__ float red[kMergeThreads / 32];
   __shared__ float4 acc_sh[NGRP][TPG];
+  // launched to start while the split kernel ends: its partials are read only
+  // after that kernel has completed
+  pdl_wait();
   const int row = blockIdx.x;  // (s * qlen + new token) * Hq + query head
   const int s = row / (p.Hq * p.qlen);
   const int lmax = min(p.maxB * p.bs, p.Pmax * p.partition_size);
@@ -92,11 +96,20 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const DecodePa
 
 cudaError_t launch_lse_merge(const DecodeParams& p, int head_dim, cudaStream_t st) {
   const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.S) * p.qlen * p.Hq);
-  if (head_dim == 64)
-    lse_merge_kernel<64><<<grid, kMergeThreads, 0, st>>>(p);
-  else
-    lse_merge_kernel<128><<<grid, kMergeThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge's CTAs are set up while the split
+  // kernel before it on the stream finishes, and wait for its partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return head_dim == 64 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, p)
+                        : cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, p);
 }
 
 }  // namespace pa
