@@ -31,10 +31,10 @@
 //       unnormalised partial and its (m, l) to the split workspace); with
 //       E4M3 caches also the converter that widens each 8-bit K/V tile to
 //       16 bits in shared memory (and rounds bf16 q to f16);
-//   warp 12     TMA: each item's query tile (two buffers) and the 128-token K
+//   warp 13     TMA: each item's query tile (two buffers) and the 128-token K
 //       tiles, block by block through the block table, into the K ring;
 //   warp 15     TMA: the V tiles into the V ring;
-//   warp 13     the Q.K^T issuer; warp 14 the P.V issuer.
+//   warp 12     the Q.K^T issuer; warp 14 the P.V issuer.
 // Every mbarrier wait gives up after about one second (error bit); a warp
 // that gives up raises a shared abort flag that stops the others, and
 // in-flight MMAs and TMA loads are drained (bounded) before the tensor
@@ -60,7 +60,10 @@ constexpr int kErrLayout = 0x10;
 
 constexpr int kHalfBytes = kTcRows * 128;  // 64 channels (128 bytes) of 128 rows
 constexpr int kStageOff = kHalfBytes;      // E4M3 tile inside a ring slot (see slot_bytes)
-constexpr int kKProdWarp = 12, kSWarp = 13, kPvWarp = 14, kVProdWarp = 15;
+// the K producer sits on its own sub-partition (warp % 4 = 1) rather than on
+// the one of the first softmax rows, which are the only live ones of a
+// narrow decode group
+constexpr int kKProdWarp = 13, kSWarp = 12, kPvWarp = 14, kVProdWarp = 15;
 // tensor memory columns
 constexpr uint32_t kTmS = 0, kTmP = 256, kTmO = 384;
 // mbarriers (8 bytes each): q full / empty / converted per q buffer; S full
@@ -282,8 +285,9 @@ struct Cursor {
 // KIND: 0 f16 q and caches, 1 bf16 q and caches, 2 f16 q with E4M3 caches,
 // 3 bf16 q with E4M3 caches (an instantiation per kind keeps each one's
 // code to its own path: the warps of six roles share an SM's instruction
-// caches).
-template <int D, int KIND>
+// caches).  NARROW: a launch whose query tiles hold at most 96 rows (a decode
+// group), whose softmax warps without a live row skip the arithmetic.
+template <int D, int KIND, bool NARROW>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kKProdWarp || warp == kVProdWarp) {
     // ============================ TMA producers ============================
-    // warp 12: the query tiles and the K tiles; warp 15: the V tiles.  Lane i
+    // warp 13: the query tiles and the K tiles; warp 15: the V tiles.  Lane i
     // issues box i of a tile: 64-channel half i % HALVES of block i / HALVES
     // (one box of D bytes per block for E4M3); a tile has at most
     // 128 / 8 blocks x 2 halves = 32 boxes.
@@ -673,6 +677,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const Item it = item_of(p, seq_tab, len_tab, tabs, k);
       if (!it.valid || it.ntiles == 0) continue;
       const bool live = r < it.ntok * p.G;
+      const bool dead = NARROW && (warp & 3) * 32 >= it.ntok * p.G;  // all 32 rows past the item's rows
       const int pos = live ? it.L - p.C + it.j0 + r / p.G : -1;
       const int last = min(pos, it.kv_hi - 1);  // last token this row attends to
       float sl2 = p.scale_log2;                 // this row's score multiplier (base 2)
@@ -693,6 +698,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const int b = g & 1, ph = (g >> 1) & 1;
         if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarSFull + b), ph)))) break;
+        if (dead) {
+          // no row of this warp is a query of the item (a decode group of
+          // fewer than 128 rows): only the arrivals, in the same order, and
+          // the waits that keep them to one phase at a time; P and O of these
+          // rows are never read into an output
+          mbar_arrive(bar(kBarSFree + b));
+          xchg[b * 2 * kTcRows + hh * kTcRows + r] = -CUDART_INF_F;
+          mbar_arrive(bar(kBarXchg + b));
+          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarXchg + b), ph)))) break;
+          mbar_arrive(bar(kBarPFull + b));
+          continue;
+        }
         tc_fence_after();
         float sv[64];
         tmem_ld32(tS + 128u * b, *reinterpret_cast<float(*)[32]>(sv));
@@ -1009,7 +1026,7 @@ template <int D, int KIND>
 cudaError_t launch_d(const TcParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                      int grid, int smem, cudaStream_t st) {
   // every warp role fits in the 128 registers a thread of the 512 gets
-  auto kern = attn_tc_kernel<D, KIND>;
+  auto kern = p.n_qt == 1 && p.C * p.G <= 96 ? attn_tc_kernel<D, KIND, true> : attn_tc_kernel<D, KIND, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kTcThreads, smem, st>>>(tmQ, tmK, tmV, p);
