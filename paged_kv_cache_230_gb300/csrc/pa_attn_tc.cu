@@ -287,6 +287,53 @@ struct Cursor {
 // code to its own path: the warps of six roles share an SM's instruction
 // caches).  NARROW: a launch whose query tiles hold at most 96 rows (a decode
 // group), whose softmax warps without a live row skip the arithmetic.
+// Row r of an E4M3 tile landed at s16 + kStageOff, widened exactly to f16 in
+// the 128-byte-swizzled operand layout of the 16-bit tile at s16 (rows at or
+// past `valid` become zeros, so that 0 * junk cannot make NaN in P.V).  For
+// head_dim 128 in place: the 8-bit row r sits where the second channel half
+// of 16-bit row r goes, and it is read whole before any of it is written.
+// Out of line: one copy serves the K and the V tiles.
+template <int D>
+__device__ __noinline__ void widen_row(uint32_t s16, int r, int valid) {
+  const uint32_t s8 = s16 + kStageOff;
+  const int rsw = r & 7;
+  if constexpr (D == 128) {
+    uint4 in[8];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+      in[cc] = r < valid ? ld_shared_v4(s8 + r * 128 + ((cc ^ rsw) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {  // 16 channels: 16-bit chunks 2 cc, 2 cc + 1 of the row
+      uint32_t h[8];
+      e4m3x4_to_f16(in[cc].x, h[0], h[1]);
+      e4m3x4_to_f16(in[cc].y, h[2], h[3]);
+      e4m3x4_to_f16(in[cc].z, h[4], h[5]);
+      e4m3x4_to_f16(in[cc].w, h[6], h[7]);
+      const uint32_t rowa = s16 + (cc >> 2) * kHalfBytes + r * 128;
+      const int jj = 2 * (cc & 3);
+      st_shared_v4(rowa + ((jj ^ rsw) << 4), h[0], h[1], h[2], h[3]);
+      st_shared_v4(rowa + (((jj + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
+    }
+  } else {
+    uint4 in[4];
+    const int rsw64 = (r >> 1) & 3;  // 64-byte swizzle of the 8-bit rows
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+      in[cc] = r < valid ? ld_shared_v4(s8 + r * 64 + ((cc ^ rsw64) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t h[8];
+      e4m3x4_to_f16(in[cc].x, h[0], h[1]);
+      e4m3x4_to_f16(in[cc].y, h[2], h[3]);
+      e4m3x4_to_f16(in[cc].z, h[4], h[5]);
+      e4m3x4_to_f16(in[cc].w, h[6], h[7]);
+      const uint32_t rowa = s16 + r * 128;
+      st_shared_v4(rowa + (((2 * cc) ^ rsw) << 4), h[0], h[1], h[2], h[3]);
+      st_shared_v4(rowa + (((2 * cc + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
 template <int D, int KIND, bool NARROW>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -924,46 +971,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
       };
       // one landed tile, widened in place (its 16-bit tile at s16)
-      auto convert = [&](const Cursor& c, uint32_t s16) {
-        const int valid = valid_tokens(c.it, c.t);
-        const uint32_t s8 = s16 + kStageOff;
-        const int rsw = r & 7;
-        if constexpr (D == 128) {
-          uint4 in[8];
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            in[cc] = r < valid ? ld_shared_v4(s8 + r * 128 + ((cc ^ rsw) << 4)) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {  // 16 channels: 16-bit chunks 2 cc, 2 cc + 1 of the row
-            uint32_t h[8];
-            e4m3x4_to_f16(in[cc].x, h[0], h[1]);
-            e4m3x4_to_f16(in[cc].y, h[2], h[3]);
-            e4m3x4_to_f16(in[cc].z, h[4], h[5]);
-            e4m3x4_to_f16(in[cc].w, h[6], h[7]);
-            const uint32_t rowa = s16 + (cc >> 2) * kHalfBytes + r * 128;
-            const int jj = 2 * (cc & 3);
-            st_shared_v4(rowa + ((jj ^ rsw) << 4), h[0], h[1], h[2], h[3]);
-            st_shared_v4(rowa + (((jj + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
-          }
-        } else {
-          uint4 in[4];
-          const int rsw64 = (r >> 1) & 3;  // 64-byte swizzle of the 8-bit rows
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            in[cc] = r < valid ? ld_shared_v4(s8 + r * 64 + ((cc ^ rsw64) << 4)) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t h[8];
-            e4m3x4_to_f16(in[cc].x, h[0], h[1]);
-            e4m3x4_to_f16(in[cc].y, h[2], h[3]);
-            e4m3x4_to_f16(in[cc].z, h[4], h[5]);
-            e4m3x4_to_f16(in[cc].w, h[6], h[7]);
-            const uint32_t rowa = s16 + r * 128;
-            st_shared_v4(rowa + (((2 * cc) ^ rsw) << 4), h[0], h[1], h[2], h[3]);
-            st_shared_v4(rowa + (((2 * cc + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
-          }
-        }
-      };
+      auto convert = [&](const Cursor& c, uint32_t s16) { widen_row<D>(s16, r, valid_tokens(c.it, c.t)); };
       // the tiles in the order K(0), K(1), then V(j), K(j + 2) for j = 0, 1,
       // ...; an item's outputs once its last V tile is widened
       Cursor kc, vc;
