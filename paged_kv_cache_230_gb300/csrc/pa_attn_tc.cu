@@ -230,8 +230,11 @@ struct Item {
 // Work item k of this CTA (global index item_index(p, k)).  With
 // at most kTcMaxRanked items per CTA their sequences and context lengths
 // come from the tables built at start-up (shared memory, no global load on
-// the pipeline's path).
-__device__ Item item_of(const TcParams& p, const int* seq_tab, const int* len_tab, bool tabs, int k) {
+// the pipeline's path).  Out of line: every warp role looks items up at its
+// item boundaries, and one copy of this code instead of one per role leaves
+// more of the instruction caches to the loops (E4M3 prefill 702 -> 823
+// TFLOP/s, k = 8 decode 324 -> 315 us).
+__device__ __noinline__ Item item_of(const TcParams& p, const int* seq_tab, const int* len_tab, bool tabs, int k) {
   Item it;
   const int idx = item_index(p, k);
   const int per_h = p.n_qt * p.R;
@@ -332,6 +335,86 @@ __device__ __noinline__ void widen_row(uint32_t s16, int r, int valid) {
       st_shared_v4(rowa + (((2 * cc + 1) ^ rsw) << 4), h[4], h[5], h[6], h[7]);
     }
   }
+}
+
+// The outputs of item `it` (or its split partials) from the epilogue thread
+// of row r: the context-length check (once per sequence), then, once the
+// item's last P.V has completed (O full) and the softmax has handed over the
+// row's (l, m), O / l from tensor memory to the output in the q dtype, or the
+// unnormalised partial and its (m, l) to the split workspace; O and the
+// (l, m) slots are released to the next item after the last tensor-memory
+// read.  ord: the item's ordinal among those with tiles (the phase parity of
+// O full and l ready).  False on a failed wait.  (Kept inline: out of line it
+// measured slower.)
+template <int D, bool kOutBf16>
+__device__ __forceinline__ bool write_item_out(const TcParams& p, const Item& it, int r, uint32_t tO, uint32_t bar0,
+                                            volatile int* abort_flag, const float* l_buf, const float* m_buf,
+                                            int ord) {
+  auto bar = [&](int k) -> uint32_t { return bar0 + 8u * k; };
+  if (r == 0 && it.h == 0 && it.run == 0 && it.qt == p.n_qt - 1) {  // once per sequence
+    const int L = __ldg(p.context_lens + it.s);
+    if (L != it.L) atomicOr(p.err, kErrContextLen);  // negative, or past the table (or partitions)
+  }
+  if (!it.valid) return true;
+  const bool live = r < it.ntok * p.G;
+  const int j = it.j0 + r / p.G;
+  const int64_t row = (static_cast<int64_t>(it.s) * p.C + j) * p.Hq + it.h * p.G + r % p.G;
+  const bool have = it.ntiles > 0;
+  float l = 0.f, m = -CUDART_INF_F;
+  if (have) {
+    // the epilogue idles through most of an item: poll with a pause (at most
+    // about 50 ms) so that it takes few issue slots from the softmax warps,
+    // then the usual bounded wait
+    for (int spin = 0; spin < 400000 && !mbar_try_wait(bar(kBarOFull), ord & 1); ++spin) __nanosleep(128);
+    const bool got = !*abort_flag && __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFull), ord & 1)) &&
+                     __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarLReady), ord & 1));
+    if (!got) return false;
+    tc_fence_after();
+    l = l_buf[r] + l_buf[kTcRows + r];
+    m = m_buf[r];
+  }
+  const float inv = l > 0.f ? p.vscale / l : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    float o[32];
+    if (have) {
+      tmem_ld32(tO + 32 * c, o);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    }
+    if (c == D / 32 - 1 && have) {
+      // O and the (l, m) slots may take the next item's
+      tc_fence_before();
+      mbar_arrive(bar(kBarOFree));
+    }
+    if (!live) continue;
+    if (it.final_out) {
+      uint16_t* orow = static_cast<uint16_t*>(p.out) + row * D + c * 32;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 w;
+        w.x = pack16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv, kOutBf16);
+        w.y = pack16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv, kOutBf16);
+        w.z = pack16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv, kOutBf16);
+        w.w = pack16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv, kOutBf16);
+        *reinterpret_cast<uint4*>(orow + q4 * 8) = w;
+      }
+    } else {
+      float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.Pmax + it.run) * D + c * 32);
+      const float vs = p.vscale;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        dst[q4] = make_float4(o[4 * q4] * vs, o[4 * q4 + 1] * vs, o[4 * q4 + 2] * vs, o[4 * q4 + 3] * vs);
+    }
+  }
+  if (live && !it.final_out) {
+    const int64_t slot = row * p.Pmax + it.run;
+    p.ws_ml[2 * slot] = l > 0.f ? m : -CUDART_INF_F;
+    p.ws_ml[2 * slot + 1] = l;
+  }
+  return true;
 }
 
 template <int D, int KIND, bool NARROW>
@@ -849,72 +932,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the outputs of item k (or its split partials)
     auto epilogue = [&](int k) -> bool {
       const Item it = item_of(p, seq_tab, len_tab, tabs, k);
-      if (r == 0 && it.h == 0 && it.run == 0 && it.qt == p.n_qt - 1) {  // once per sequence
-        const int L = __ldg(p.context_lens + it.s);
-        if (L != it.L) atomicOr(p.err, kErrContextLen);  // negative, or past the table (or partitions)
-      }
-      if (!it.valid) return true;
-      const bool live = r < it.ntok * p.G;
-      const int j = it.j0 + r / p.G;
-      const int64_t row = (static_cast<int64_t>(it.s) * p.C + j) * p.Hq + it.h * p.G + r % p.G;
-      const bool have = it.ntiles > 0;
-      float l = 0.f, m = -CUDART_INF_F;
-      if (have) {
-        // the epilogue idles through most of an item: poll with a pause (at
-        // most about 50 ms) so that it takes few issue slots from the
-        // softmax warps, then the usual bounded wait
-        for (int spin = 0; spin < 400000 && !mbar_try_wait(bar(kBarOFull), ord & 1); ++spin) __nanosleep(128);
-        const bool got = !*abort_flag && __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFull), ord & 1)) &&
-                         __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarLReady), ord & 1));
-        if (!got) return false;
-        tc_fence_after();
-        l = l_buf[r] + l_buf[kTcRows + r];
-        m = m_buf[r];
-      }
-      const float inv = l > 0.f ? p.vscale / l : 0.f;
-      // a rolled loop: once per item, and its code shares the instruction
-      // caches with the converter's and the softmax's
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        if (have) {
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
-        }
-        if (c == D / 32 - 1 && have) {
-          // O and the (l, m) slots may take the next item's
-          tc_fence_before();
-          mbar_arrive(bar(kBarOFree));
-        }
-        if (!live) continue;
-        if (it.final_out) {
-          uint16_t* orow = static_cast<uint16_t*>(p.out) + row * D + c * 32;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv, kOutBf16);
-            w.y = pack16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv, kOutBf16);
-            w.z = pack16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv, kOutBf16);
-            w.w = pack16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv, kOutBf16);
-            *reinterpret_cast<uint4*>(orow + q4 * 8) = w;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.Pmax + it.run) * D + c * 32);
-          const float vs = p.vscale;
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(o[4 * q4] * vs, o[4 * q4 + 1] * vs, o[4 * q4 + 2] * vs, o[4 * q4 + 3] * vs);
-        }
-      }
-      if (live && !it.final_out) {
-        const int64_t slot = row * p.Pmax + it.run;
-        p.ws_ml[2 * slot] = l > 0.f ? m : -CUDART_INF_F;
-        p.ws_ml[2 * slot + 1] = l;
-      }
-      if (have) ++ord;
+      if (!write_item_out<D, kOutBf16>(p, it, r, tO, bar0, abort_flag, l_buf, m_buf, ord)) return false;
+      if (it.valid && it.ntiles > 0) ++ord;
       return true;
     };
     if (!kFp8) {
