@@ -304,3 +304,31 @@ def test_concurrent_launches_on_many_streams_agree():
     assert pa.get_device_error() == 0
     for o in outs:
         assert torch.equal(o, ref)
+
+
+NARROW_EDGES = [
+    # (Hq, Hkv, G x k rows): the narrow instantiation serves groups of at most
+    # 96 rows, its softmax warps with no live row (rows 32 w .. 32 w + 31 all
+    # past the group) skipping the arithmetic
+    (32, 8, 8),    # G = 4, k = 8: 32 rows, warps 1-3 of each half without a live row
+    (33, 1, 1),    # G = 33, k = 1: 33 rows, one live row in the second quarter
+    (16, 1, 4),    # G = 16, k = 4: 64 rows
+    (32, 1, 3),    # G = 32, k = 3: 96 rows, the largest narrow group
+    (97, 1, 1),    # G = 97: 97 rows, the smallest group past the narrow instantiation
+]
+
+
+@pytest.mark.parametrize("P", [0, 128])
+@pytest.mark.parametrize("case", NARROW_EDGES, ids=lambda c: "Hq%d-Hkv%d-k%d" % c)
+def test_narrow_group_edges(case, P):
+    Hq, Hkv, k = case
+    wl = W.make_workload(name="t", seed=68, context_lens=[1, 5, 129, 700, 1500], Hq=Hq, Hkv=Hkv, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="bf16", qlen=k)
+    pa = _gpu.lib()
+    g = _gpu.OnGpu(wl)
+    out = g.step(partition_size=P).clone()
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    kc, vc = _gpu.oracle_pool(wl)
+    assert _gpu.max_err(out, _gpu.oracle_out(wl, kc, vc, partition_size=P)) <= _gpu.tolerance(wl)
+    _check_zero_rows(out, wl)
