@@ -207,7 +207,7 @@ DECODE_SOURCES = ("pa_decode.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_decode_f16
 TC_SOURCES = ("pa_attn_tc.cu", "pa_attn_tc.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
 
 
-PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill_pair.cu", "pa_prefill.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
 
 
 def kernel_source_hash(sources=DECODE_SOURCES) -> str:
@@ -684,10 +684,14 @@ def run_prefill(args, local):
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
     flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())
-    # 16-bit head_dim-128 caches go to the per-head kernel, E4M3 caches and
-    # head_dim 64 to the tensor-core kernel with the GQA heads packed in rows
+    # 16-bit head_dim-128 caches go to the per-head kernels (two query heads
+    # per work item for an even group size), E4M3 caches and head_dim 64 to
+    # the tensor-core kernel with the GQA heads packed in rows
     per_head = kv != W.FP8 and wl.D == 128
-    kernel = "pa_prefill (prefill_kernel)" if per_head else "pa_prefill (attn_tc_kernel)"
+    if per_head:
+        kernel = "pa_prefill (prefill_pair_kernel)" if (wl.Hq // wl.Hkv) % 2 == 0 else "pa_prefill (prefill_kernel)"
+    else:
+        kernel = "pa_prefill (attn_tc_kernel)"
     sources = PREFILL_SOURCES if per_head else TC_SOURCES
 
     def run():

@@ -158,10 +158,12 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * queries of a (sequence, kv head) are packed as rows token * G + head,
  * floor(128 / G) tokens x G heads per 128-row tile, so every K/V tile loaded
  * serves all G heads (the kernel of the wide-group decode calls).  With
- * 16-bit caches and head_dim 128 a work item is (sequence, query head, 128
- * new tokens) of a kernel built for that shape, which measured faster there.
- * Both are persistent, one CTA per SM walking the items (longest contexts
- * first), and stream each item's 128-token K/V tiles through the block table.
+ * 16-bit caches and head_dim 128 a work item is (sequence, two query heads of
+ * one kv head, 128 new tokens) for an even G, whose two query tiles share
+ * each K/V tile, or (sequence, query head, 128 new tokens) for an odd G: the
+ * kernels built for that shape, which measured faster there.  All are
+ * persistent, one CTA per SM walking the items, and stream each item's
+ * 128-token K/V tiles through the block table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
  * Supported: head_dim 64 or 128, caches of the q dtype or FP8 E4M3, block
  * size 8, 16 or 32, G up to 128, scale > 0.  E4M3 tiles are widened exactly

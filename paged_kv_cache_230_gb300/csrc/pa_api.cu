@@ -385,9 +385,10 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
   return finish(e, st);
 }
 
-// Chunked prefill with 16-bit caches and head_dim 128 through the per-head
-// persistent kernel (pa_prefill.cu): work items (sequence, query head, 128
-// new tokens).  Arguments are checked by the caller.
+// Chunked prefill with 16-bit caches and head_dim 128 through a persistent
+// kernel: work items (sequence, pair of query heads of one kv head, 128 new
+// tokens) for an even group size (pa_prefill_pair.cu), else (sequence, query
+// head, 128 new tokens) (pa_prefill.cu).  Arguments are checked by the caller.
 int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
   const pa_cache_desc* cache = a.cache;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.qlen;
@@ -426,7 +427,9 @@ int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
   p.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return finish(pa::launch_prefill(p, tq, tk, tv, st), st);
+  // an even group: two query heads per work item share each K/V tile
+  const bool pair = p.G % 2 == 0;
+  return finish(pair ? pa::launch_prefill_pair(p, tq, tk, tv, st) : pa::launch_prefill(p, tq, tk, tv, st), st);
 }
 
 }  // namespace

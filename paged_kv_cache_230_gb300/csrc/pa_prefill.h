@@ -28,4 +28,10 @@ struct PrefillParams {
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t st);
 
+// The same with two query heads of one kv head per work item (an even group
+// size G): their query tiles share each K/V tile, and their MMAs alternate
+// (pa_prefill_pair.cu).  Same maps and parameters.
+cudaError_t launch_prefill_pair(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                const CUtensorMap& tmV, cudaStream_t st);
+
 }  // namespace pa
