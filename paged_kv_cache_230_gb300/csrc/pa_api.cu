@@ -209,7 +209,13 @@ cudaError_t launch_decode(const pa::DecodeParams& p, const CUtensorMap& tk, cons
 // Pmax partitions, so launch and pipeline ramp costs are paid per run, not
 // per partition.
 #ifndef PA_SPLIT_CTAS_PER_SLOT
-#define PA_SPLIT_CTAS_PER_SLOT 16
+#define PA_SPLIT_CTAS_PER_SLOT 8
+#endif
+// The last partitions of every context run one per CTA, after all the longer
+// runs: the launch then ends on short runs instead of a partial wave of long
+// ones.
+#ifndef PA_SPLIT_FRINGE
+#define PA_SPLIT_FRINGE 8
 #endif
 std::atomic<int> g_sm_count[kMaxDevices];
 
@@ -586,6 +592,7 @@ int decode_split_impl(const DecodeArgs& a, int32_t max_context_len, int32_t part
   p.partition_size = partition_size;
   p.Pmax = static_cast<int>(np);
   p.parts_per_cta = parts_per_cta(a.num_seqs, cache->num_kv_heads, p.Pmax);
+  p.fringe = p.parts_per_cta > 1 ? static_cast<int>(std::min<int64_t>(PA_SPLIT_FRINGE, p.Pmax)) : 0;
   const size_t rows = static_cast<size_t>(a.num_seqs) * a.qlen * a.num_q_heads * np;
   // partial outputs first: their rows of head_dim floats keep the 16-byte
   // alignment of the workspace for the merge's vector loads

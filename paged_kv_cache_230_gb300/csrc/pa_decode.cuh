@@ -395,31 +395,65 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- which (sequence, kv head, run of partitions) ----
-  // Split variant: CTA c of a (sequence, kv head) owns partitions
-  // [c * ppc, (c + 1) * ppc) and streams them back to back.
+  // Split variant: the grid's first S * Hkv * nb CTAs take the bulk runs (CTA
+  // c of a (sequence, kv head) streams partitions [c * ppc, (c + 1) * ppc) of
+  // the context's first P - F back to back), the last S * Hkv * F CTAs the
+  // fringe: each of a context's last F partitions alone.  CTAs start roughly
+  // in index order, so the runs that end the launch are single partitions.
   const bool split = p.partition_size > 0;
-  const int nchunk = split ? (p.Pmax + p.parts_per_cta - 1) / p.parts_per_cta : 1;
+  const int F = split ? p.fringe : 0;
+  const int nb = split ? split_bulk_ctas(p.Pmax, F, p.parts_per_cta) : 1;
   int bid = blockIdx.x;
-  const int chunk = bid % nchunk;
-  bid /= nchunk;
+  const bool fringe = bid >= p.S * p.Hkv * nb;
+  int chunk;  // bulk run index, or fringe index j in [0, F)
+  if (!fringe) {
+    chunk = bid % nb;
+    bid /= nb;
+  } else {
+    bid -= p.S * p.Hkv * nb;
+    chunk = bid % F;
+    bid /= F;
+  }
   const int h = bid % p.Hkv;
   const int s = p.S > 1 ? seq_of_rank(p.context_lens, p.S, bid / p.Hkv) : 0;
   int lmax = p.maxB * p.bs;
   if (split) lmax = min(lmax, p.Pmax * p.partition_size);
   int L = p.context_lens[s];
+  // the first CTA of the (sequence, kv head 0): bulk run 0, or the last fringe
+  // CTA when there is no bulk
+  const bool lead = h == 0 && (nb > 0 ? !fringe && chunk == 0 : chunk == F - 1);
   if (L < 0 || L > lmax) {
-    if (tid == 0 && chunk == 0 && h == 0) atomicOr(p.err, kErrContextLen);
+    if (tid == 0 && lead) atomicOr(p.err, kErrContextLen);
     L = min(max(L, 0), lmax);
   }
-  int tok_begin = 0, tok_end = L, part_first = 0;
+  int tok_begin = 0, tok_end = L, run = 0, nruns = 1;
   if (split) {
-    part_first = chunk * p.parts_per_cta;
-    tok_begin = part_first * p.partition_size;
-    tok_end = min(L, (part_first + p.parts_per_cta) * p.partition_size);
-    if (chunk > 0 && tok_begin >= L) return;  // past the end of this context
+    const int ps = p.partition_size, ppc = p.parts_per_cta;
+    const int P = (L + ps - 1) / ps;
+    const int bulk_end = max(P - F, 0);
+    nruns = split_runs(P, F, ppc);
+    // an empty context is one empty run: bulk run 0, or the last fringe CTA
+    // without a fringe
+    const bool empty_owner = P == 0 && (F == 0 ? !fringe && chunk == 0 : fringe && chunk == F - 1);
+    int first = 0, last = 0;  // partitions [first, last)
+    if (!empty_owner) {
+      if (!fringe) {
+        first = chunk * ppc;
+        if (first >= bulk_end) return;  // past this context's bulk
+        last = min(first + ppc, bulk_end);
+        run = chunk;
+      } else {
+        first = P - F + chunk;
+        if (first < 0) return;  // the context has fewer than F partitions
+        last = first + 1;
+        run = (bulk_end + ppc - 1) / ppc + (first - bulk_end);
+      }
+    }
+    tok_begin = first * ps;
+    tok_end = min(L, last * ps);
   }
   // this CTA holds every partition of the context: it writes the final output
-  const bool final_out = !split || L <= p.parts_per_cta * p.partition_size;
+  const bool final_out = !split || nruns == 1;
   const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TILE - 1) / TILE : 0;
   const int tiles_per_seg = split ? p.partition_size / TILE : max(ntiles, 1);
 
@@ -622,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           }
         }
       }
-      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, chunk},
+      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, run},
                               vscale, [&](bool first) {
         // with split columns, the first warp in order that owns a column
         // (cw 0 or 1) initialises it and the other (cw 2 or 3) adds
@@ -865,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           ml[(cw * NG + g) * 2 + 1] = l_run[g];
         }
       }
-      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, chunk},
+      segment_epilogue<D, NG>(p, cw, ctid, area, carea, cml, ml, s, h, SegInfo{seg, last, split, final_out, run},
                               vscale, [&](bool first) {
         if (grp == 0) {
 #pragma unroll
@@ -982,7 +1016,7 @@ cudaError_t launch_one(const DecodeParams& p0, const CUtensorMap& tmK, const CUt
   auto kern = decode_kernel<KV, D, USE_MMA, NG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int nchunk = split ? (p.Pmax + p.parts_per_cta - 1) / p.parts_per_cta : 1;
+  const int nchunk = split ? split_bulk_ctas(p.Pmax, p.fringe, p.parts_per_cta) + p.fringe : 1;
   const long long grid = static_cast<long long>(p.S) * p.Hkv * nchunk;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmK, tmV, p);
   return cudaGetLastError();

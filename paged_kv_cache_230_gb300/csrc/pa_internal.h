@@ -38,6 +38,7 @@ struct DecodeParams {
   int partition_size;         // tokens per partition; 0 = whole context per CTA
   int Pmax;                   // partitions per sequence (1 without split)
   int parts_per_cta;          // split: consecutive partitions streamed by one CTA
+  int fringe;                 // split: a context's last partitions run one per CTA
   int nst;                    // ring stages (set by the launcher)
   float scale_log2;           // scale * log2(e)
   float kv_scale;             // FP8 dequantisation scale (1 for 16-bit caches)
@@ -48,6 +49,21 @@ struct DecodeParams {
   void* k_cache;              // the pool, written through plain stores
   void* v_cache;
 };
+
+// Runs of a split context of P partitions: its first max(P - F, 0)
+// partitions in runs of ppc consecutive ones, its last min(P, F) one per run
+// (the fringe); an empty context is one empty run.  Run r's partial is
+// workspace slot r of each of the context's query rows.
+__host__ __device__ inline int split_runs(int P, int F, int ppc) {
+  const int bulk = P > F ? P - F : 0;
+  const int n = (bulk + ppc - 1) / ppc + (P < F ? P : F);
+  return n > 1 ? n : 1;
+}
+// Split CTAs per (sequence, kv head) in the grid: the bulk runs of the
+// longest context, then F fringe runs.
+__host__ __device__ inline int split_bulk_ctas(int Pmax, int F, int ppc) {
+  return ((Pmax > F ? Pmax - F : 0) + ppc - 1) / ppc;
+}
 
 // Launches the decode (or split-partition) kernel for one cache dtype.
 // tmK/tmV: 4-D tensor maps over [NB, Hkv, bs, D] with the box and swizzle that

@@ -17,6 +17,10 @@ CASES = [
     (8, 2, "bf16", 16, 256, [256, 300, 1000, 129]),
     (4, 1, "f16", 8, 192, [192, 450, 64]),
     (2, 2, "bf16", 32, 320, [320, 333, 1500]),
+    # even groups take the two-head kernel: G = 2 (one pair) and G = 8 (four
+    # pairs), several query tiles, a ragged last tile
+    (4, 2, "bf16", 16, 640, [640, 700, 2000]),
+    (16, 2, "f16", 32, 200, [1500, 201]),
 ]
 
 
