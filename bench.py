@@ -684,12 +684,13 @@ def run_prefill(args, local):
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
     flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())
-    # 16-bit head_dim-128 caches go to the per-head kernels (two query heads
-    # per work item for an even group size), E4M3 caches and head_dim 64 to
-    # the tensor-core kernel with the GQA heads packed in rows
-    per_head = kv != W.FP8 and wl.D == 128
+    # 16-bit caches go to the head-pair kernel for an even group size (head_dim
+    # 64 or 128) or the one-head kernel (head_dim 128); E4M3 caches to the
+    # tensor-core kernel with the GQA heads packed in rows
+    even = (wl.Hq // wl.Hkv) % 2 == 0
+    per_head = kv != W.FP8 and (even or wl.D == 128)
     if per_head:
-        kernel = "pa_prefill (prefill_pair_kernel)" if (wl.Hq // wl.Hkv) % 2 == 0 else "pa_prefill (prefill_kernel)"
+        kernel = "pa_prefill (prefill_pair_kernel)" if even else "pa_prefill (prefill_kernel)"
     else:
         kernel = "pa_prefill (attn_tc_kernel)"
     sources = PREFILL_SOURCES if per_head else TC_SOURCES

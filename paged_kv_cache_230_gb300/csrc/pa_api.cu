@@ -391,10 +391,11 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
   return finish(e, st);
 }
 
-// Chunked prefill with 16-bit caches and head_dim 128 through a persistent
-// kernel: work items (sequence, pair of query heads of one kv head, 128 new
-// tokens) for an even group size (pa_prefill_pair.cu), else (sequence, query
-// head, 128 new tokens) (pa_prefill.cu).  Arguments are checked by the caller.
+// Chunked prefill with 16-bit caches through a persistent kernel: work items
+// (sequence, pair of query heads of one kv head, 128 new tokens) for an even
+// group size and head_dim 64 or 128 (pa_prefill_pair.cu), else (sequence,
+// query head, 128 new tokens) with head_dim 128 (pa_prefill.cu).  Arguments
+// are checked by the caller.
 int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
   const pa_cache_desc* cache = a.cache;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.qlen;
@@ -408,9 +409,10 @@ int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
     return rc;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
-  // q as {128 channels, heads, tokens}; box = 64 channels x 1 head x 128 tokens
-  const cuuint64_t dims[3] = {128, cuuint64_t(a.num_q_heads), cuuint64_t(rows)};
-  const cuuint64_t strides[2] = {256, cuuint64_t(a.num_q_heads) * 256};
+  // q as {D channels, heads, tokens}; box = 64 channels x 1 head x 128 tokens
+  const int D = cache->head_dim;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(a.num_q_heads), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(a.num_q_heads) * D * 2};
   const cuuint32_t box[3] = {64, 1, cuuint32_t(pa::kPfRows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
@@ -430,6 +432,7 @@ int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
   p.G = a.num_q_heads / cache->num_kv_heads;
   p.bs = cache->block_size;
   p.maxB = a.max_blocks_per_seq;
+  p.D = D;
   p.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -543,7 +546,10 @@ int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int3
   if (!out || !q || !block_tables || !context_lens || !aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
   const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
-  if (cache->kv_dtype != PA_FP8_E4M3 && cache->head_dim == 128) return prefill_per_head_impl(a, stream);
+  // 16-bit caches: the head-pair kernel for an even group (head_dim 64 or
+  // 128), the one-head kernel for an odd group with head_dim 128
+  const int G = num_q_heads / cache->num_kv_heads;
+  if (cache->kv_dtype != PA_FP8_E4M3 && (G % 2 == 0 || cache->head_dim == 128)) return prefill_per_head_impl(a, stream);
   return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
 }
 

@@ -13,23 +13,24 @@ constexpr int kPfStages = 2;     // K/V tiles in flight
 constexpr int kPfThreads = 384;  // softmax, epilogue and TMA/MMA warpgroups
 
 struct PrefillParams {
-  void* out;                    // [S, C, Hq, 128] of the cache dtype
+  void* out;                    // [S, C, Hq, D] of the cache dtype
   const int32_t* block_tables;  // [S, maxB]
   const int32_t* context_lens;  // [S] (includes the C new tokens)
   int* err;                     // device error word
   int64_t num_blocks;
   int S, C, Hq, Hkv, G, bs, maxB;
+  int D;                        // head_dim: 128 (both kernels) or 64 (two-head kernel)
   int bf16;                     // 1: bf16 operands, 0: f16
   float scale_log2;             // softmax scale * log2(e)
 };
 
-// tmQ: 3-D map over q {128 channels, Hq, S*C tokens}, box {64, 1, 128};
+// tmQ: 3-D map over q {D channels, Hq, S*C tokens}, box {64, 1, 128};
 // tmK/tmV: the caches' 4-D maps (box {64, bs, 1, 1}), 128-byte swizzle.
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t st);
 
 // The same with two query heads of one kv head per work item (an even group
-// size G): their query tiles share each K/V tile, and their MMAs alternate
+// size G; head_dim 64 or 128): their query tiles share each K/V tile
 // (pa_prefill_pair.cu).  Same maps and parameters.
 cudaError_t launch_prefill_pair(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                 const CUtensorMap& tmV, cudaStream_t st);

@@ -52,9 +52,15 @@ constexpr int kErrLayout = 0x10;
 
 constexpr int kRows = 128, kTok = 128, kThreads = 512;
 constexpr int kHalf = kRows * 128;  // 64 channels (128 bytes) of 128 rows
-constexpr int kTileB = 2 * kHalf;   // 128 rows x 128 channels of 16 bits
-// shared memory: the query tiles a and b, two K slots, two V slots, the tail
-constexpr int kQOff = 0, kKOff = 2 * kTileB, kVOff = kKOff + 2 * kTileB, kTailOff = kVOff + 2 * kTileB;
+// Per head_dim D: a tile (128 rows x D channels of 16 bits) is D / 64
+// segments of kHalf; shared memory holds the query tiles a and b, two K
+// slots, two V slots, then the tail.
+template <int D>
+struct Geo {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileB = kHalves * kHalf;
+  static constexpr int kQOff = 0, kKOff = 2 * kTileB, kVOff = kKOff + 2 * kTileB, kTailOff = kVOff + 2 * kTileB;
+};
 // mbarriers: q full / empty; S full, P full and P.V done of a and of b; O
 // full / free; l ready; full / empty per K slot and per V slot; one drain
 // barrier per issuer
@@ -62,11 +68,13 @@ constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarSFull = 2, kBarPFull = 4, kBarP
               kBarOFree = 9, kBarLReady = 10, kBarKFull = 11, kBarKEmpty = 13, kBarVFull = 15, kBarVEmpty = 17,
               kBarDrain = 19, kNumBars = 21;
 constexpr int kAbortOff = kNumBars * 8, kTmemOff = kAbortOff + 4, kLOff = kTmemOff + 4;
-constexpr int kSmemBytes = kTailOff + kLOff + 2 * kRows * 4;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+template <int D>
+constexpr int smem_bytes() { return Geo<D>::kTailOff + kLOff + 2 * kRows * 4; }
+static_assert(smem_bytes<128>() <= 227 * 1024, "shared memory budget");
 // tensor memory columns of S and O of tile x (0: a, 1: b)
 __host__ __device__ constexpr uint32_t tm_s(int x) { return x ? 128u : 0u; }
-__host__ __device__ constexpr uint32_t tm_o(int x) { return x ? 384u : 256u; }
+template <int D>
+__host__ __device__ constexpr uint32_t tm_o(int x) { return 256u + static_cast<uint32_t>(x * D); }
 // A row's reference max moves only when a tile exceeds it by more than this
 // (base 2): probabilities stay below 2^8 and O is rescaled rarely.
 constexpr float kRescaleThreshold = 8.f;
@@ -171,11 +179,14 @@ __device__ __noinline__ PairItem pair_item(const PrefillParams& p, int idx, int 
   return it;
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  using Gm = Geo<D>;
+  constexpr int kTileB = Gm::kTileB, kQOff = Gm::kQOff, kKOff = Gm::kKOff, kVOff = Gm::kVOff,
+                kTailOff = Gm::kTailOff;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = smem_u32(smem);
   if (base & 1023u) {  // the swizzled operand tiles need 1024-byte alignment
@@ -249,11 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 13 || warp == 15) {
     // ============================ TMA producers ============================
     // warp 13: the query tiles and the K tiles; warp 15: the V tiles.  Lane i
-    // issues box i of a tile: 64-channel half i % 2 of block i / 2 (at most
-    // 128 / 8 blocks x 2 halves = 32 boxes).
+    // issues box i of a tile: 64-channel segment i % (D / 64) of block
+    // i / (D / 64) (at most 128 / 8 blocks x 2 segments = 32 boxes).
     const bool is_k = warp == 13;
     const CUtensorMap* map = is_k ? &tmK : &tmV;
-    const int my_blk = lane >> 1, my_half = lane & 1;
+    const int my_blk = lane / Gm::kHalves, my_half = lane % Gm::kHalves;
     const uint32_t ring = base + (is_k ? kKOff : kVOff);
     const int full_bar = is_k ? kBarKFull : kBarVFull, empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
     if (lane == 0) {
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int x = 0; x < 2; ++x)
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
+            for (int hf = 0; hf < Gm::kHalves; ++hf)
               tma_load_3d(base + kQOff + x * kTileB + hf * kHalf, &tmQ, full, 64 * hf, head + x, row);
         }
         __syncwarp();
@@ -295,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b0 = t * bpt;
         const int nb = min(bpt, nblk - b0);
         const uint32_t full = bar(full_bar + slot);
-        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * p.bs * 256));
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * p.bs * D * 2));
         __syncwarp();
         const int phys = pre;
         if (t + 1 < it.ntiles) pre = my_blk < min(bpt, nblk - b0 - bpt) ? __ldg(bt_row + b0 + bpt + my_blk) : -1;
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t qd = tc_desc_sw128(base + kQOff + x * kTileB, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
               mma_ss(tmem + tm_s(x), qd + off, kd + off, idesc, kk > 0);
             }
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 14) {
     // ================== P.V issuer (one warp), a and b alternating ==================
-    const uint32_t idesc = tc_idesc_f16(BF16, true, kRows, 128);
+    const uint32_t idesc = tc_idesc_f16(BF16, true, kRows, D);
     int g = 0, ord = 0;
     bool ok = true;
     PairItem it;
@@ -373,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // rows past the context in the last k-step hold pool bytes past the
           // context or stale tiles: zero them so that 0 * junk cannot make NaN
           const int rows = nks * 16 - valid;
-          for (int w = lane; w < rows * 16; w += 32) {
-            const int row = valid + w / 16, rest = w % 16;
+          constexpr int kPieces = D / 8;  // 16-byte pieces of a row
+          for (int w = lane; w < rows * kPieces; w += 32) {
+            const int row = valid + w / kPieces, rest = w % kPieces;
             st_shared_v4(vb + (rest / 8) * kHalf + row * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
@@ -391,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               if (kk < nks)
-                mma_ts(tmem + tm_o(x), tmem + tm_s(x) + 64 + 8 * kk, vd + ((kk * 2048) >> 4), idesc,
+                mma_ts(tmem + tm_o<D>(x), tmem + tm_s(x) + 64 + 8 * kk, vd + ((kk * 2048) >> 4), idesc,
                        kk > 0 ? 1u : acc0);
             }
             tc_commit(bar(kBarPvDone + x));
@@ -420,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid & 127;   // row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + tm_s(x) + lane_off;
-    const uint32_t tO = tmem + tm_o(x) + lane_off;
+    const uint32_t tO = tmem + tm_o<D>(x) + lane_off;
     const float sl2 = p.scale_log2;
     int g = 0, ord = 0;
     bool ok = true;
@@ -484,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // rows whose reference moved rescale their O row (no P.V into it
           // is in flight: S_x(g) was issued after P_x(g - 1).V completed)
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             float o[32];
             tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
@@ -534,18 +546,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int head = it.h * p.G + 2 * it.hp + x;
         uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                         ((static_cast<int64_t>(it.s) * p.C + it.i0 + r) * p.Hq + head) * 128;
+                         ((static_cast<int64_t>(it.s) * p.C + it.i0 + r) * p.Hq + head) * D;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           float o[32];
           if (have) {
-            tmem_ld32(tmem + tm_o(x) + lane_off + 32 * c, o);
+            tmem_ld32(tmem + tm_o<D>(x) + lane_off + 32 * c, o);
             tmem_wait_ld();
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = 0.f;
           }
-          if (x == 1 && c == 3 && have) {
+          if (x == 1 && c == D / 32 - 1 && have) {
             // O and the l slots may take the next item's
             tc_fence_before();
             mbar_arrive(bar(kBarOFree));
@@ -575,10 +587,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, int grid, cudaStream_t st) {
-  auto kern = prefill_pair_kernel<BF16>;
+  auto kern = prefill_pair_kernel<D, BF16>;
+  // at least half an SM's shared memory, so that no two CTAs share an SM
+  // (each allocates all 512 TMEM columns; a second one would wait for them)
+  constexpr int kSmemBytes = smem_bytes<D>() > 116 * 1024 ? smem_bytes<D>() : 116 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // the warpgroups' setmaxnreg shares must fit in the registers the CTA is
@@ -601,7 +616,7 @@ cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tmQ, const 
 
 cudaError_t launch_prefill_pair(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                 const CUtensorMap& tmV, cudaStream_t st) {
-  if (p.G < 2 || (p.G & 1) || p.S <= 0 || p.C <= 0) return cudaErrorInvalidValue;
+  if (p.G < 2 || (p.G & 1) || p.S <= 0 || p.C <= 0 || (p.D != 64 && p.D != 128)) return cudaErrorInvalidValue;
   static std::atomic<int> sms[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
@@ -615,7 +630,9 @@ cudaError_t launch_prefill_pair(const PrefillParams& p, const CUtensorMap& tmQ, 
   if (total > INT32_MAX) return cudaErrorInvalidValue;
   // persistent: one CTA per SM (all of its tensor memory)
   const int grid = static_cast<int>(total < nsm ? total : nsm);
-  return p.bf16 ? launch_pair_t<true>(p, tmQ, tmK, tmV, grid, st) : launch_pair_t<false>(p, tmQ, tmK, tmV, grid, st);
+  if (p.D == 64)
+    return p.bf16 ? launch_pair_t<64, true>(p, tmQ, tmK, tmV, grid, st) : launch_pair_t<64, false>(p, tmQ, tmK, tmV, grid, st);
+  return p.bf16 ? launch_pair_t<128, true>(p, tmQ, tmK, tmV, grid, st) : launch_pair_t<128, false>(p, tmQ, tmK, tmV, grid, st);
 }
 
 }  // namespace pa

@@ -28,14 +28,17 @@ def _check_zero_rows(out, wl):
 
 
 PREFILL = [
-    # (Hq, Hkv, D, dtype, bs, C, context lengths)
-    (8, 2, 64, "bf16", 16, 256, [256, 300, 1000, 129]),
-    (4, 4, 64, "f16", 8, 200, [200, 201, 777]),
-    (12, 4, 128, "bf16", 16, 300, [300, 650, 1200]),    # G = 3: 42 tokens x 3 heads per tile
-    (24, 4, 64, "f16", 32, 100, [100, 400]),            # G = 6
-    (64, 4, 128, "bf16", 16, 70, [70, 500, 1300]),      # G = 16: 8 tokens per tile
+    # (Hq, Hkv, D, dtype, bs, C, context lengths).  16-bit caches: an even
+    # group takes the head-pair kernel (head_dim 64 or 128), an odd one the
+    # one-head kernel (head_dim 128) or the packed-group kernel (head_dim 64)
+    (8, 2, 64, "bf16", 16, 256, [256, 300, 1000, 129]),  # G = 4, two pairs
+    (4, 4, 64, "f16", 8, 200, [200, 201, 777]),          # G = 1, packed
+    (12, 4, 128, "bf16", 16, 300, [300, 650, 1200]),    # G = 3, one head per item
+    (24, 4, 64, "f16", 32, 100, [100, 400]),            # G = 6, three pairs
+    (64, 4, 128, "bf16", 16, 70, [70, 500, 1300]),      # G = 16, eight pairs
     (32, 1, 128, "f16", 16, 40, [40, 333]),             # G = 32 (MQA)
-    (128, 1, 64, "bf16", 8, 9, [9, 100, 257]),          # G = 128: one token per tile
+    (128, 1, 64, "bf16", 8, 9, [9, 100, 257]),          # G = 128, 64 pairs
+    (12, 4, 64, "bf16", 16, 130, [130, 700]),           # G = 3, packed
 ]
 
 
