@@ -207,7 +207,8 @@ DECODE_SOURCES = ("pa_decode.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_decode_f16
 TC_SOURCES = ("pa_attn_tc.cu", "pa_attn_tc.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
 
 
-PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill_pair.cu", "pa_prefill.h", "pa_tcgen05.cuh", "pa_ptx.cuh")
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_prefill_pair.cu", "pa_prefill.h", "pa_widen.cu", "pa_widen.h", "pa_tcgen05.cuh",
+                   "pa_ptx.cuh")
 
 
 def kernel_source_hash(sources=DECODE_SOURCES) -> str:
@@ -684,13 +685,16 @@ def run_prefill(args, local):
     b = DeviceBatch(wl, "cuda")
     pos = np.arange(L - C, L, dtype=np.float64)
     flops = 4.0 * wl.D * wl.Hq * S * float((pos + 1).sum())
-    # 16-bit caches go to the head-pair kernel for an even group size (head_dim
-    # 64 or 128) or the one-head kernel (head_dim 128); E4M3 caches to the
-    # tensor-core kernel with the GQA heads packed in rows
+    # an even group goes to the head-pair kernel (head_dim 64 or 128; E4M3
+    # caches widened to the q dtype first), an odd one to the one-head kernel
+    # (16-bit, head_dim 128) or the tensor-core kernel with the GQA heads
+    # packed in rows
     even = (wl.Hq // wl.Hkv) % 2 == 0
-    per_head = kv != W.FP8 and (even or wl.D == 128)
-    if per_head:
-        kernel = "pa_prefill (prefill_pair_kernel)" if even else "pa_prefill (prefill_kernel)"
+    per_head = even or (kv != W.FP8 and wl.D == 128)
+    if even:
+        kernel = "pa_prefill (widen_kv_kernel, prefill_pair_kernel)" if kv == W.FP8 else "pa_prefill (prefill_pair_kernel)"
+    elif per_head:
+        kernel = "pa_prefill (prefill_kernel)"
     else:
         kernel = "pa_prefill (attn_tc_kernel)"
     sources = PREFILL_SOURCES if per_head else TC_SOURCES
@@ -734,8 +738,9 @@ def run_prefill(args, local):
     burst, _ = measured_tensor_peak()
     line = {"metric": "paged prefill attention TFLOP/s (causal FLOPs)", "value": tflops, "unit": "TFLOP/s",
             "n_gpus": 1, "steps": K, "warmup": args.warmup, "higher_is_better": True,
-            # E4M3 tiles are widened to f16 in shared memory: the MMAs run in f16
-            "dtype": "f16" if kv == W.FP8 else "bf16",
+            # E4M3 blocks are widened exactly to the q dtype (bf16) for the
+            # head-pair kernel; the packed-group kernel widens them to f16
+            "dtype": "bf16" if (even or kv != W.FP8) else "f16",
             "data": "synthetic", "config": {"workload": wl.name, "num_seqs": S, "chunk": C, "context": L,
                                             "q_heads": 32, "kv_heads": 8, "head_dim": wl.D, "block_size": bs,
                                             "kv_dtype": wl.kv_dtype},

@@ -154,23 +154,29 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * num_q_tokens new tokens per sequence (positions L - C .. L - 1 of each
  * context; chunked prefill, review §10 table), computed on the tensor cores
  * with tcgen05 MMAs and tensor-memory accumulators: prefill is the
- * compute-bound phase (review §7).  With E4M3 caches or head_dim 64 the
- * queries of a (sequence, kv head) are packed as rows token * G + head,
- * floor(128 / G) tokens x G heads per 128-row tile, so every K/V tile loaded
- * serves all G heads (the kernel of the wide-group decode calls).  With
- * 16-bit caches and head_dim 128 a work item is (sequence, two query heads of
- * one kv head, 128 new tokens) for an even G, whose two query tiles share
- * each K/V tile, or (sequence, query head, 128 new tokens) for an odd G: the
- * kernels built for that shape, which measured faster there.  All are
- * persistent, one CTA per SM walking the items, and stream each item's
- * 128-token K/V tiles through the block table.
+ * compute-bound phase (review §7).  For an even group size G a work item
+ * is (sequence, two query heads of one kv head, 128 new tokens): the two
+ * query tiles share each K/V tile loaded.  With E4M3 caches the batch's
+ * blocks are first widened exactly to the q dtype (every E4M3 value is a
+ * bf16 and an f16 value) into scratch from a library-owned, stream-ordered
+ * memory pool: 4 * num_kv_heads * block_size * head_dim + 4 bytes per entry
+ * of the block tables ([num_seqs, max_blocks_per_seq]), returned to the pool
+ * (which keeps it reserved for the next call) once the call's kernels are
+ * done; kv_scale then multiplies the scores and the output.  For an odd G,
+ * 16-bit caches with head_dim 128 take work items (sequence, query head, 128
+ * new tokens); the other odd-G calls (and an even G whose scratch cannot be
+ * allocated) pack the queries of a (sequence, kv head) as rows token * G +
+ * head, floor(128 / G) tokens x G heads per 128-row tile, so every K/V tile
+ * loaded serves all G heads (the kernel of the wide-group decode calls);
+ * there E4M3 tiles are widened to f16 in shared memory and the MMAs run in
+ * f16, bf16 q scaled per query row by a power of two 2^e (max|q| 2^e in
+ * [2^14, 2^15)) and rounded to f16, exact but for entries below 2^-29 of the
+ * row's largest.  All kernels are persistent, one CTA per SM walking the
+ * items, and stream each item's 128-token K/V tiles through the block table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
  * Supported: head_dim 64 or 128, caches of the q dtype or FP8 E4M3, block
- * size 8, 16 or 32, G up to 128, scale > 0.  E4M3 tiles are widened exactly
- * to f16 in shared memory and the MMAs run in f16; bf16 q is then scaled per
- * query row by a power of two 2^e (max|q| 2^e in [2^14, 2^15)) and rounded
- * to f16, exact but for entries below 2^-29 of the row's largest.  Other
- * arguments as pa_decode (kv_scale must be 1 for 16-bit caches).
+ * size 8, 16 or 32, G up to 128, scale > 0.  Other arguments as pa_decode
+ * (kv_scale must be 1 for 16-bit caches).
  */
 PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                       int32_t num_q_heads, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,

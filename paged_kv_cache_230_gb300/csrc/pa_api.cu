@@ -10,6 +10,7 @@
 #include "pa_attn_tc.h"
 #include "pa_internal.h"
 #include "pa_prefill.h"
+#include "pa_widen.h"
 
 namespace {
 
@@ -396,7 +397,7 @@ int attn_tc_impl(const DecodeArgs& a, int32_t max_context_len, int32_t partition
 // group size and head_dim 64 or 128 (pa_prefill_pair.cu), else (sequence,
 // query head, 128 new tokens) with head_dim 128 (pa_prefill.cu).  Arguments
 // are checked by the caller.
-int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
+int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream, float vscale = 1.f) {
   const pa_cache_desc* cache = a.cache;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.qlen;
   const int64_t nqt = (a.qlen + pa::kPfRows - 1) / pa::kPfRows;
@@ -435,10 +436,94 @@ int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream) {
   p.D = D;
   p.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.vscale = vscale;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // an even group: two query heads per work item share each K/V tile
   const bool pair = p.G % 2 == 0;
   return finish(pair ? pa::launch_prefill_pair(p, tq, tk, tv, st) : pa::launch_prefill(p, tq, tk, tv, st), st);
+}
+
+// A memory pool per device for the widened blocks of FP8 prefill: freed
+// scratch stays reserved in it (release threshold unlimited), so a call
+// after the first reuses the memory instead of mapping it again.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices];
+bool g_pool_made[kMaxDevices];
+
+cudaMemPool_t scratch_pool() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if (!g_pool_made[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_pool[dev] = pool;
+    g_pool_made[dev] = true;
+  }
+  return g_pool[dev];
+}
+
+// Prefill over E4M3 caches with an even group: the batch's blocks are widened
+// exactly to the query's 16-bit type into stream-ordered scratch (a compact
+// pool with its own block table: 4 * Hkv * bs * D bytes per table entry, plus
+// the table), then the head-pair kernel runs on it with the per-tensor scale
+// on the scores and the output.  Returns 1 when the scratch cannot be had
+// (the caller then takes the packed-group kernel).
+int prefill_fp8_pair_impl(const DecodeArgs& a, pa_stream_t stream) {
+  const pa_cache_desc* cache = a.cache;
+  const int64_t nslot = static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq;
+  const int64_t blk = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim;  // elements
+  if (nslot > INT32_MAX) return 1;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  cudaMemPool_t pool = scratch_pool();
+  if (!pool) return 1;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t kv_bytes = static_cast<size_t>(nslot * blk * 2);  // one of K, V widened
+  void* ws = nullptr;
+  if (cudaMallocFromPoolAsync(&ws, 2 * kv_bytes + static_cast<size_t>(nslot) * 4, pool, st) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  pa::WidenParams w{};
+  w.k_src = static_cast<const uint8_t*>(a.k_cache);
+  w.v_src = static_cast<const uint8_t*>(a.v_cache);
+  w.k_dst = static_cast<uint16_t*>(ws);
+  w.v_dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + kv_bytes);
+  w.tab = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + 2 * kv_bytes);
+  w.block_tables = a.block_tables;
+  w.context_lens = a.context_lens;
+  w.err = err;
+  w.num_blocks = cache->num_blocks;
+  w.S = a.num_seqs;
+  w.maxB = a.max_blocks_per_seq;
+  w.Hkv = cache->num_kv_heads;
+  w.bs = cache->block_size;
+  w.D = cache->head_dim;
+  w.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+  int rc = PA_OK;
+  if (pa::launch_widen_kv(w, st) != cudaSuccess) {
+    rc = PA_ERR_CUDA;
+  } else {
+    pa_cache_desc wide = *cache;
+    wide.kv_dtype = a.q_dtype;
+    wide.num_blocks = nslot;
+    DecodeArgs b = a;
+    b.k_cache = w.k_dst;
+    b.v_cache = w.v_dst;
+    b.cache = &wide;
+    b.block_tables = w.tab;
+    b.scale = a.scale * a.kv_scale;
+    rc = prefill_per_head_impl(b, stream, a.kv_scale);
+  }
+  cudaFreeAsync(ws, st);
+  return rc;
 }
 
 }  // namespace
@@ -550,6 +635,11 @@ int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int3
   // 128), the one-head kernel for an odd group with head_dim 128
   const int G = num_q_heads / cache->num_kv_heads;
   if (cache->kv_dtype != PA_FP8_E4M3 && (G % 2 == 0 || cache->head_dim == 128)) return prefill_per_head_impl(a, stream);
+  // E4M3 caches with an even group: widened, then the head-pair kernel
+  if (cache->kv_dtype == PA_FP8_E4M3 && G % 2 == 0) {
+    const int r = prefill_fp8_pair_impl(a, stream);
+    if (r != 1) return r;
+  }
   return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
 }
 

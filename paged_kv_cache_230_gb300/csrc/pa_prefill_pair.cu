@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int x = 0; x < 2; ++x) {
         const float l = have ? l_buf[x * kRows + r] : 0.f;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? p.vscale / l : 0.f;
         const int head = it.h * p.G + 2 * it.hp + x;
         uint16_t* orow = static_cast<uint16_t*>(p.out) +
                          ((static_cast<int64_t>(it.s) * p.C + it.i0 + r) * p.Hq + head) * D;
