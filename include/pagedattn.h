@@ -156,15 +156,15 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * with tcgen05 MMAs and tensor-memory accumulators: prefill is the
  * compute-bound phase (review §7).  For an even group size G a work item
  * is (sequence, two query heads of one kv head, 128 new tokens): the two
- * query tiles share each K/V tile loaded.  With E4M3 caches the batch's
- * blocks are first widened exactly to the q dtype (every E4M3 value is a
- * bf16 and an f16 value) into scratch from a library-owned, stream-ordered
+ * query tiles share each K/V tile loaded; for an odd G with head_dim 128 it
+ * is (sequence, query head, 128 new tokens).  With E4M3 caches those calls
+ * first widen the batch's blocks exactly to the q dtype (every E4M3 value is
+ * a bf16 and an f16 value) into scratch from a library-owned, stream-ordered
  * memory pool: 4 * num_kv_heads * block_size * head_dim + 4 bytes per entry
  * of the block tables ([num_seqs, max_blocks_per_seq]), returned to the pool
  * (which keeps it reserved for the next call) once the call's kernels are
- * done; kv_scale then multiplies the scores and the output.  For an odd G,
- * 16-bit caches with head_dim 128 take work items (sequence, query head, 128
- * new tokens); the other odd-G calls (and an even G whose scratch cannot be
+ * done; kv_scale then multiplies the scores and the output.  The other calls
+ * (an odd G with head_dim 64, or E4M3 caches whose scratch cannot be
  * allocated) pack the queries of a (sequence, kv head) as rows token * G +
  * head, floor(128 / G) tokens x G heads per 128-row tile, so every K/V tile
  * loaded serves all G heads (the kernel of the wide-group decode calls);

@@ -469,13 +469,13 @@ cudaMemPool_t scratch_pool() {
   return g_pool[dev];
 }
 
-// Prefill over E4M3 caches with an even group: the batch's blocks are widened
-// exactly to the query's 16-bit type into stream-ordered scratch (a compact
-// pool with its own block table: 4 * Hkv * bs * D bytes per table entry, plus
-// the table), then the head-pair kernel runs on it with the per-tensor scale
-// on the scores and the output.  Returns 1 when the scratch cannot be had
-// (the caller then takes the packed-group kernel).
-int prefill_fp8_pair_impl(const DecodeArgs& a, pa_stream_t stream) {
+// Prefill over E4M3 caches: the batch's blocks are widened exactly to the
+// query's 16-bit type into stream-ordered scratch (a compact pool with its
+// own block table: 4 * Hkv * bs * D bytes per table entry, plus the table),
+// then the 16-bit prefill kernels run on it with the per-tensor scale on the
+// scores and the output.  Returns 1 when the scratch cannot be had (the
+// caller then takes the packed-group kernel).
+int prefill_fp8_widened_impl(const DecodeArgs& a, pa_stream_t stream) {
   const pa_cache_desc* cache = a.cache;
   const int64_t nslot = static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq;
   const int64_t blk = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim;  // elements
@@ -635,9 +635,10 @@ int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int3
   // 128), the one-head kernel for an odd group with head_dim 128
   const int G = num_q_heads / cache->num_kv_heads;
   if (cache->kv_dtype != PA_FP8_E4M3 && (G % 2 == 0 || cache->head_dim == 128)) return prefill_per_head_impl(a, stream);
-  // E4M3 caches with an even group: widened, then the head-pair kernel
-  if (cache->kv_dtype == PA_FP8_E4M3 && G % 2 == 0) {
-    const int r = prefill_fp8_pair_impl(a, stream);
+  // E4M3 caches: widened, then the same kernels (an odd group with head_dim
+  // 64 stays with the packed-group kernel, which widens in shared memory)
+  if (cache->kv_dtype == PA_FP8_E4M3 && (G % 2 == 0 || cache->head_dim == 128)) {
+    const int r = prefill_fp8_widened_impl(a, stream);
     if (r != 1) return r;
   }
   return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);

@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (ok) {
           tc_fence_after();
           const float l = l_buf[(k & 1) * kPfRows + r];
-          inv = l > 0.f ? 1.f / l : 0.f;
+          inv = l > 0.f ? p.vscale / l : 0.f;
           have = true;
         }
       }

@@ -22,8 +22,7 @@ struct PrefillParams {
   int D;                        // head_dim: 128 (both kernels) or 64 (two-head kernel)
   int bf16;                     // 1: bf16 operands, 0: f16
   float scale_log2;             // softmax scale * log2(e)
-  float vscale;                 // output factor (the E4M3 per-tensor scale; 1 for 16-bit caches;
-                                // the two-head kernel only)
+  float vscale;                 // output factor (the E4M3 per-tensor scale; 1 for 16-bit caches)
 };
 
 // tmQ: 3-D map over q {D channels, Hq, S*C tokens}, box {64, 1, 128};
