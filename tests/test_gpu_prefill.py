@@ -186,3 +186,35 @@ def test_out_of_range_block_ids_are_contained_and_reported():
     # the sequence that never touches the bad entry is unaffected
     base = _prefill(g, wl)
     assert torch.equal(out[0], base[0])
+
+
+def _prefill_fp8(g, wl, bt=None):
+    out = torch.full_like(g.q, float("nan"))
+    _gpu.lib().prefill(out, g.q, g.kc, g.vc, g.bt if bt is None else bt, g.cl, wl.scale, wl.kv_scale)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("Hq", [8, 6], ids=["G4", "G3"])
+def test_fp8_widened_blocks_with_nan_slots_and_bad_ids(Hq):
+    """E4M3 caches through the widening pass (head_dim 128, an even and an odd
+    group): pool slots past every context hold the E4M3 NaN code, a block id
+    out of range is contained and reported, and a sequence that never touches
+    it is unaffected."""
+    pa = _gpu.lib()
+    wl = W.make_workload(name="t", seed=47, context_lens=[200, 300, 17], Hq=Hq, Hkv=2, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="fp8", qlen=130, fill_unused="nan")
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    assert pa.get_device_error() == 0
+    base = _prefill_fp8(g, wl)
+    assert pa.get_device_error() == 0
+    kc, vc = _gpu.oracle_pool(wl)
+    assert _gpu.max_err(base, _gpu.oracle_out(wl, kc, vc)) <= _gpu.tolerance(wl)
+    bad = g.bt.clone()
+    bad[1, 3] = wl.NB + 5
+    out = _prefill_fp8(g, wl, bt=bad)
+    assert pa.get_device_error() & pa.DEVERR_BLOCK_ID
+    assert pa.get_device_error() == 0  # reading clears it
+    assert torch.isfinite(out.float()).all()
+    assert torch.equal(out[0], base[0]) and torch.equal(out[2], base[2])
