@@ -24,8 +24,9 @@
 //       previous P.V has completed;
 //   warp 13     TMA: the item's two query tiles and the 128-token K tiles,
 //       block by block through the block table, into a 2-slot ring;
-//   warp 14     issues O_a += P_a(j) V(j), then O_b += P_b(j) V(j), each once
-//       the tile's softmax has stored P;
+//   warp 14     issues O_a += P_a(j) V(j), then O_b += P_b(j) V(j), the MMAs
+//       of each half of the keys once the softmax has stored that half of P
+//       (so P.V runs while the softmax finishes the row);
 //   warp 15     TMA: the V tiles into a 2-slot ring.
 // Every mbarrier wait gives up after about one second (error bit); a warp that
 // gives up raises a shared abort flag that stops the others, and in-flight
@@ -61,12 +62,14 @@ struct Geo {
   static constexpr int kTileB = kHalves * kHalf;
   static constexpr int kQOff = 0, kKOff = 2 * kTileB, kVOff = kKOff + 2 * kTileB, kTailOff = kVOff + 2 * kTileB;
 };
-// mbarriers: q full / empty; S full, P full and P.V done of a and of b; O
+// mbarriers: q full / empty; S full of a and of b; P full of each half of
+// the keys of a and of b (head_dim 64: the first of each pair only); P.V done
+// of a and of b; O
 // full / free; l ready; full / empty per K slot and per V slot; one drain
 // barrier per issuer
-constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarSFull = 2, kBarPFull = 4, kBarPvDone = 6, kBarOFull = 8,
-              kBarOFree = 9, kBarLReady = 10, kBarKFull = 11, kBarKEmpty = 13, kBarVFull = 15, kBarVEmpty = 17,
-              kBarDrain = 19, kNumBars = 21;
+constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarSFull = 2, kBarPFull = 4, kBarPvDone = 8, kBarOFull = 10,
+              kBarOFree = 11, kBarLReady = 12, kBarKFull = 13, kBarKEmpty = 15, kBarVFull = 17, kBarVEmpty = 19,
+              kBarDrain = 21, kNumBars = 23;
 constexpr int kAbortOff = kNumBars * 8, kTmemOff = kAbortOff + 4, kLOff = kTmemOff + 4;
 template <int D>
 constexpr int smem_bytes() { return Geo<D>::kTailOff + kLOff + 2 * kRows * 4; }
@@ -213,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarQEmpty), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(kBarSFull + x), 1);
-      mbar_init(bar(kBarPFull + x), kRows);
+      mbar_init(bar(kBarPFull + 2 * x), kRows);
+      mbar_init(bar(kBarPFull + 2 * x + 1), kRows);
       mbar_init(bar(kBarPvDone + x), 1);
     }
     mbar_init(bar(kBarOFull), 1);
@@ -396,19 +400,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0 && ord >= 1 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarOFree), (ord - 1) & 1)))) break;
         const uint64_t vd = tc_desc_sw128(vb, kHalf, 1024);
         const uint32_t acc0 = t > 0 ? 1u : 0u;
-        for (int x = 0; x < 2; ++x) {
-          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPFull + x), g & 1)))) break;
-          tc_fence_after();
-          if (lane == 0) {
+        for (int x = 0; x < 2 && ok; ++x) {
+          // head_dim 128: P_x(g) arrives in two halves of the keys, and the
+          // MMAs of a half go out as soon as it is stored; head_dim 64: all at once
+          constexpr int kParts = D == 128 ? 2 : 1;
+          for (int h = 0; h < kParts; ++h) {
+            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarPFull + 2 * x + h), g & 1)))) break;
+            tc_fence_after();
+            if (lane == 0) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              if (kk < nks)
-                mma_ts(tmem + tm_o<D>(x), tmem + tm_s(x) + 64 + 8 * kk, vd + ((kk * 2048) >> 4), idesc,
-                       kk > 0 ? 1u : acc0);
+              for (int k = 0; k < 8 / kParts; ++k) {
+                const int kk = (8 / kParts) * h + k;
+                if (kk < nks)
+                  mma_ts(tmem + tm_o<D>(x), tmem + tm_s(x) + 64 + 8 * kk, vd + ((kk * 2048) >> 4), idesc,
+                         kk > 0 ? 1u : acc0);
+              }
+              if (h == kParts - 1) tc_commit(bar(kBarPvDone + x));
             }
-            tc_commit(bar(kBarPvDone + x));
+            __syncwarp();
           }
-          __syncwarp();
         }
         if (!ok) break;
         if (lane == 0) {
@@ -474,9 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-m_use, -m_use);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         // P as 16-bit pairs, 16 words (32 columns) at a time, over S columns
-        // 64..127 (all read above)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        // 64..127 (all read above), then the row sum
+        auto exps_store = [&](int c) {
           uint32_t pw[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -487,27 +496,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             pw[e >> 1] = pack16<BF16>(e0, e1);
           }
           tmem_st16(tS + 64 + 16 * c, pw);
+        };
+        // rows whose reference moved rescale their O row (no P.V into it is
+        // in flight: S_x(g) was issued after P_x(g - 1).V completed, and
+        // P_x(g).V starts at the first arrival on P full below)
+        auto rescale_o = [&]() {
+          if (t > 0 && __any_sync(0xFFFFFFFFu, bump)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tmem_ld32(tO + 32 * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_st32(tO + 32 * c, o);
+            }
+          }
+        };
+        if constexpr (D == 128) {
+          // each half of the keys released to the P.V issuer once stored, so
+          // P.V runs while the softmax finishes the row
+          rescale_o();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            exps_store(c);
+            if (c & 1) {
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(bar(kBarPFull + 2 * x + (c >> 1)));
+            }
+          }
+        } else {
+          // head_dim 64 (half the P.V work): all of P at once, which measured
+          // faster there
+#pragma unroll
+          for (int c = 0; c < 4; ++c) exps_store(c);
+          rescale_o();
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(kBarPFull + 2 * x));
         }
         float sum8[8];
 #pragma unroll
         for (int a = 0; a < 4; ++a) f2unpack(acc[a], sum8[2 * a], sum8[2 * a + 1]);
         l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
-        if (t > 0 && __any_sync(0xFFFFFFFFu, bump)) {
-          // rows whose reference moved rescale their O row (no P.V into it
-          // is in flight: S_x(g) was issued after P_x(g - 1).V completed)
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tO + 32 * c, o);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kBarPFull + x));
       }
       if (!ok) break;
       // hand l to the epilogue; the slots were read by the previous item's
