@@ -64,12 +64,12 @@ struct Geo {
 };
 // mbarriers: q full / empty; S full of a and of b; P full of each half of
 // the keys of a and of b (head_dim 64: the first of each pair only); P.V done
-// of a and of b; O
-// full / free; l ready; full / empty per K slot and per V slot; one drain
-// barrier per issuer
+// of a and of b; O full / free; l ready; full / empty per K slot and per V
+// slot; one drain barrier per issuer; S read by the softmax, of a and of b
+// (head_dim 64)
 constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarSFull = 2, kBarPFull = 4, kBarPvDone = 8, kBarOFull = 10,
               kBarOFree = 11, kBarLReady = 12, kBarKFull = 13, kBarKEmpty = 15, kBarVFull = 17, kBarVEmpty = 19,
-              kBarDrain = 21, kNumBars = 23;
+              kBarDrain = 21, kBarSRead = 23, kNumBars = 25;
 constexpr int kAbortOff = kNumBars * 8, kTmemOff = kAbortOff + 4, kLOff = kTmemOff + 4;
 template <int D>
 constexpr int smem_bytes() { return Geo<D>::kTailOff + kLOff + 2 * kRows * 4; }
@@ -83,8 +83,13 @@ __host__ __device__ constexpr uint32_t tm_o(int x) { return 256u + static_cast<u
 constexpr float kRescaleThreshold = 8.f;
 // registers a thread of each warpgroup holds after setmaxnreg: two softmax
 // warpgroups, the epilogue, the TMA/MMA warps (128 x 512 = 65536 of the
-// 512 x 128 the CTA is launched with)
-constexpr int kRegsSoftmax = 176, kRegsEpilogue = 88, kRegsTmaMma = 72;
+// 512 x 128 the CTA is launched with); head_dim 64's S issue in two halves
+// needs more in the TMA/MMA warps
+template <int D>
+struct Regs {
+  static constexpr int kSoftmax = 176, kEpilogue = D == 64 ? 64 : 88, kTmaMma = D == 64 ? 96 : 72;
+  static_assert(2 * kSoftmax + kEpilogue + kTmaMma <= 512, "register shares");
+};
 
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
   uint64_t r;
@@ -219,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPFull + 2 * x), kRows);
       mbar_init(bar(kBarPFull + 2 * x + 1), kRows);
       mbar_init(bar(kBarPvDone + x), 1);
+      if constexpr (D == 64) mbar_init(bar(kBarSRead + x), kRows);
     }
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarOFree), kRows);
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a warpgroup execute the same setmaxnreg; the shares sum to at most the
   // launch's total, which the launcher checks, so the increases are granted).
   if (warp >= 12) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsTmaMma) : "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(Regs<D>::kTmaMma) : "memory");
   if (warp == 13 || warp == 15) {
     // ============================ TMA producers ============================
     // warp 13: the query tiles and the K tiles; warp 15: the V tiles.  Lane i
@@ -329,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 12) {
     // ================== Q.K^T issuer (one thread), a and b alternating ==================
     if (lane == 0) {
-      const uint32_t idesc = tc_idesc_f16(BF16, false, kRows, kTok);
+      // head_dim 64 issues S in two halves of the keys (below), head_dim 128 whole
+      constexpr bool kSplitS = D == 64;
+      const uint32_t idesc = tc_idesc_f16(BF16, false, kRows, kSplitS ? kTok / 2 : kTok);
       int g = 0, ord = 0;  // tiles and items with tiles issued
       bool ok = true;
       PairItem it;
@@ -344,14 +352,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar(kBarKFull + slot), (g >> 1) & 1))) break;
           const uint64_t kd = tc_desc_sw128(base + kKOff + slot * kTileB, 16, 1024);
           for (int x = 0; x < 2; ++x) {
-            // S_x(g) overwrites P_x(g - 1): after its P.V
-            if (g >= 1 && !(ok = mbar_wait(bar(kBarPvDone + x), (g - 1) & 1))) break;
-            tc_fence_after();
             const uint64_t qd = tc_desc_sw128(base + kQOff + x * kTileB, 16, 1024);
+            if constexpr (kSplitS) {
+              // keys 0..63 of S_x(g) go to columns 0..63, free once the
+              // softmax has read S_x(g - 1); keys 64..127 overwrite P_x(g - 1)
+              // (columns 64..127): after its P.V
+              if (g >= 1 && !(ok = mbar_wait(bar(kBarSRead + x), (g - 1) & 1))) break;
+              tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-              mma_ss(tmem + tm_s(x), qd + off, kd + off, idesc, kk > 0);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                mma_ss(tmem + tm_s(x), qd + off, kd + off, idesc, kk > 0);
+              }
+              if (g >= 1 && !(ok = mbar_wait(bar(kBarPvDone + x), (g - 1) & 1))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                mma_ss(tmem + tm_s(x) + 64, qd + off, kd + ((64 * 128) >> 4) + off, idesc, kk > 0);
+              }
+            } else {
+              // S_x(g) overwrites P_x(g - 1): after its P.V
+              if (g >= 1 && !(ok = mbar_wait(bar(kBarPvDone + x), (g - 1) & 1))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                mma_ss(tmem + tm_s(x), qd + off, kd + off, idesc, kk > 0);
+              }
             }
             tc_commit(bar(kBarSFull + x));
           }
@@ -436,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax) : "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(Regs<D>::kSoftmax) : "memory");
     // ============ softmax: one thread per (tile, row) ============
     const int x = warp >> 2;   // 0: tile a, 1: tile b
     const int r = tid & 127;   // row = TMEM lane
@@ -463,6 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
         tmem_wait_ld();
+        if constexpr (D == 64) {
+          // S_x(g) is in registers: keys 0..63 of S_x(g + 1) may overwrite columns 0..63
+          tc_fence_before();
+          mbar_arrive(bar(kBarSRead + x));
+        }
         if (!__all_sync(0xFFFFFFFFu, lim0 >= 127)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) sv[c] = (c <= lim0) ? sv[c] : -CUDART_INF_F;
@@ -549,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) fail();
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsEpilogue) : "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(Regs<D>::kEpilogue) : "memory");
     // ============ epilogue: one thread per row, both tiles ============
     const int r = tid & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -639,7 +672,8 @@ cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tmQ, const 
     regs = fa.numRegs;
     launch_regs.store(regs, std::memory_order_relaxed);
   }
-  if (128 * (2 * kRegsSoftmax + kRegsEpilogue + kRegsTmaMma) > regs * kThreads) return cudaErrorInvalidConfiguration;
+  if (128 * (2 * Regs<D>::kSoftmax + Regs<D>::kEpilogue + Regs<D>::kTmaMma) > regs * kThreads)
+    return cudaErrorInvalidConfiguration;
   kern<<<grid, kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
