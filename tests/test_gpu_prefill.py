@@ -218,3 +218,40 @@ def test_fp8_widened_blocks_with_nan_slots_and_bad_ids(Hq):
     assert pa.get_device_error() == 0  # reading clears it
     assert torch.isfinite(out.float()).all()
     assert torch.equal(out[0], base[0]) and torch.equal(out[2], base[2])
+
+
+def test_fp8_prefill_captured_in_a_graph_replays_the_eager_bits():
+    """The E4M3 prefill path allocates its widening scratch on the call's
+    stream from the library's pool; captured into a CUDA graph (allocation
+    and free become graph nodes) it replays the eager launch's bits."""
+    pa = _gpu.lib()
+    wl = W.make_workload(name="t", seed=48, context_lens=[300, 129, 700], Hq=8, Hkv=2, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="fp8", qlen=128)
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    out = torch.full_like(g.q, float("nan"))
+
+    def run():
+        pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale)
+
+    run()
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    eager = out.clone()
+    kc, vc = _gpu.oracle_pool(wl)
+    assert _gpu.max_err(eager, _gpu.oracle_out(wl, kc, vc)) <= _gpu.tolerance(wl)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 0
+        assert torch.equal(out, eager)
