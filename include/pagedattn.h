@@ -157,23 +157,26 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
  * compute-bound phase (review §7).  For an even group size G a work item
  * is (sequence, two query heads of one kv head, 128 new tokens): the two
  * query tiles share each K/V tile loaded; for an odd G with head_dim 128 it
- * is (sequence, query head, 128 new tokens).  With E4M3 caches those calls
- * first widen the batch's blocks exactly to the q dtype (every E4M3 value is
- * a bf16 and an f16 value) into scratch from a library-owned, stream-ordered
- * memory pool: 4 * num_kv_heads * block_size * head_dim + 4 bytes per entry
- * of the block tables ([num_seqs, max_blocks_per_seq]), returned to the pool
- * (which keeps it reserved for the next call) once the call's kernels are
- * done; kv_scale then multiplies the scores and the output.  The other calls
- * (an odd G with head_dim 64, or E4M3 caches whose scratch cannot be
- * allocated) pack the queries of a (sequence, kv head) as rows token * G +
- * head, floor(128 / G) tokens x G heads per 128-row tile, so every K/V tile
- * loaded serves all G heads (the kernel of the wide-group decode calls);
- * there E4M3 tiles are widened to f16 in shared memory and the MMAs run in
- * f16, bf16 q scaled per query row by a power of two 2^e (max|q| 2^e in
- * [2^14, 2^15)) and rounded to f16, exact but for entries below 2^-29 of the
- * row's largest.  All kernels are persistent, one CTA per SM walking the
- * items, and stream each item's 128-token K/V tiles through the block table.
+ * is (sequence, query head, 128 new tokens).  With E4M3 caches and a
+ * workspace (at least pa_prefill_workspace_size bytes, 16-byte aligned, owned
+ * by the caller) those calls first widen the batch's blocks exactly to the q
+ * dtype (every E4M3 value is a bf16 and an f16 value) into the workspace, a
+ * compact pool with its own block table, and kv_scale then multiplies the
+ * scores and the output.  The other calls (an odd G with head_dim 64, or
+ * E4M3 caches without a workspace) pack the queries of a (sequence, kv head)
+ * as rows token * G + head, floor(128 / G) tokens x G heads per 128-row tile,
+ * so every K/V tile loaded serves all G heads (the kernel of the wide-group
+ * decode calls); there E4M3 tiles are widened to f16 in shared memory and the
+ * MMAs run in f16, bf16 q scaled per query row by a power of two 2^e (max|q|
+ * 2^e in [2^14, 2^15)) and rounded to f16, exact but for entries below 2^-29
+ * of the row's largest.  All kernels are persistent, one CTA per SM walking
+ * the items, and stream each item's 128-token K/V tiles through the block
+ * table.
  *   out, q   [num_seqs, num_q_tokens, num_q_heads, head_dim] of q_dtype
+ *   workspace  device scratch for E4M3 caches, or NULL (ignored for 16-bit
+ *              caches); PA_ERR_WORKSPACE if non-NULL and smaller than
+ *              pa_prefill_workspace_size or not 16-byte aligned.  Its
+ *              contents are not kept between calls.
  * Supported: head_dim 64 or 128, caches of the q dtype or FP8 E4M3, block
  * size 8, 16 or 32, G up to 128, scale > 0.  Other arguments as pa_decode
  * (kv_scale must be 1 for 16-bit caches).
@@ -181,7 +184,15 @@ PA_API int pa_decode_multi(void *out, const void *q, int32_t q_dtype, int32_t nu
 PA_API int pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                       int32_t num_q_heads, const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
-                      float scale, float kv_scale, pa_stream_t stream);
+                      float scale, float kv_scale, void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Workspace bytes pa_prefill uses with E4M3 caches: 4 * num_kv_heads *
+ * block_size * head_dim + 4 per entry of the [num_seqs, max_blocks_per_seq]
+ * block tables (the widened K and V blocks and a compact table).  Returns 0
+ * for 16-bit caches and for invalid sizes.
+ */
+PA_API size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t max_blocks_per_seq, const pa_cache_desc *cache);
 
 /*
  * Workspace bytes pa_decode_split needs: num_seqs * num_q_heads *

@@ -443,60 +443,32 @@ int prefill_per_head_impl(const DecodeArgs& a, pa_stream_t stream, float vscale 
   return finish(pair ? pa::launch_prefill_pair(p, tq, tk, tv, st) : pa::launch_prefill(p, tq, tk, tv, st), st);
 }
 
-// A memory pool per device for the widened blocks of FP8 prefill: freed
-// scratch stays reserved in it (release threshold unlimited), so a call
-// after the first reuses the memory instead of mapping it again.
-std::mutex g_pool_mu;
-cudaMemPool_t g_pool[kMaxDevices];
-bool g_pool_made[kMaxDevices];
-
-cudaMemPool_t scratch_pool() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_pool_mu);
-  if (!g_pool_made[dev]) {
-    cudaMemPoolProps props = {};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
-    uint64_t keep = UINT64_MAX;
-    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    g_pool[dev] = pool;
-    g_pool_made[dev] = true;
-  }
-  return g_pool[dev];
+// Bytes of the E4M3 prefill workspace: the widened K and V blocks (2-byte
+// elements) of every block-table entry, then the compact table.
+int64_t prefill_fp8_workspace_bytes(int64_t nslot, const pa_cache_desc* c) {
+  const int64_t blk = static_cast<int64_t>(c->num_kv_heads) * c->block_size * c->head_dim;  // elements
+  return nslot * blk * 2 * 2 + nslot * 4;
 }
 
-// Prefill over E4M3 caches: the batch's blocks are widened exactly to the
-// query's 16-bit type into stream-ordered scratch (a compact pool with its
-// own block table: 4 * Hkv * bs * D bytes per table entry, plus the table),
-// then the 16-bit prefill kernels run on it with the per-tensor scale on the
-// scores and the output.  Returns 1 when the scratch cannot be had (the
-// caller then takes the packed-group kernel).
-int prefill_fp8_widened_impl(const DecodeArgs& a, pa_stream_t stream) {
+// Prefill over E4M3 caches with the caller's workspace: the batch's blocks are
+// widened exactly to the query's 16-bit type into it (a compact pool with its
+// own block table), then the 16-bit prefill kernels run on it with the
+// per-tensor scale on the scores and the output.  Arguments are checked by
+// the caller.
+int prefill_fp8_widened_impl(const DecodeArgs& a, void* workspace, pa_stream_t stream) {
   const pa_cache_desc* cache = a.cache;
   const int64_t nslot = static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq;
-  const int64_t blk = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim;  // elements
-  if (nslot > INT32_MAX) return 1;
+  if (nslot > INT32_MAX) return PA_ERR_INVALID_ARG;
   int* err = device_error_ptr();
   if (!err) return PA_ERR_CUDA;
-  cudaMemPool_t pool = scratch_pool();
-  if (!pool) return 1;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t kv_bytes = static_cast<size_t>(nslot * blk * 2);  // one of K, V widened
-  void* ws = nullptr;
-  if (cudaMallocFromPoolAsync(&ws, 2 * kv_bytes + static_cast<size_t>(nslot) * 4, pool, st) != cudaSuccess) {
-    cudaGetLastError();
-    return 1;
-  }
+  const size_t kv_bytes = static_cast<size_t>(nslot) * cache->num_kv_heads * cache->block_size * cache->head_dim * 2;
   pa::WidenParams w{};
   w.k_src = static_cast<const uint8_t*>(a.k_cache);
   w.v_src = static_cast<const uint8_t*>(a.v_cache);
-  w.k_dst = static_cast<uint16_t*>(ws);
-  w.v_dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + kv_bytes);
-  w.tab = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + 2 * kv_bytes);
+  w.k_dst = static_cast<uint16_t*>(workspace);
+  w.v_dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + kv_bytes);
+  w.tab = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + 2 * kv_bytes);
   w.block_tables = a.block_tables;
   w.context_lens = a.context_lens;
   w.err = err;
@@ -507,23 +479,17 @@ int prefill_fp8_widened_impl(const DecodeArgs& a, pa_stream_t stream) {
   w.bs = cache->block_size;
   w.D = cache->head_dim;
   w.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
-  int rc = PA_OK;
-  if (pa::launch_widen_kv(w, st) != cudaSuccess) {
-    rc = PA_ERR_CUDA;
-  } else {
-    pa_cache_desc wide = *cache;
-    wide.kv_dtype = a.q_dtype;
-    wide.num_blocks = nslot;
-    DecodeArgs b = a;
-    b.k_cache = w.k_dst;
-    b.v_cache = w.v_dst;
-    b.cache = &wide;
-    b.block_tables = w.tab;
-    b.scale = a.scale * a.kv_scale;
-    rc = prefill_per_head_impl(b, stream, a.kv_scale);
-  }
-  cudaFreeAsync(ws, st);
-  return rc;
+  if (pa::launch_widen_kv(w, st) != cudaSuccess) return finish(cudaGetLastError(), st);
+  pa_cache_desc wide = *cache;
+  wide.kv_dtype = a.q_dtype;
+  wide.num_blocks = nslot;
+  DecodeArgs b = a;
+  b.k_cache = w.k_dst;
+  b.v_cache = w.v_dst;
+  b.cache = &wide;
+  b.block_tables = w.tab;
+  b.scale = a.scale * a.kv_scale;
+  return prefill_per_head_impl(b, stream, a.kv_scale);
 }
 
 }  // namespace
@@ -612,10 +578,18 @@ int pa_decode_multi(void* out, const void* q, int32_t q_dtype, int32_t num_seqs,
   return finish(launch_decode(p, tk, tv, cache->kv_dtype, cache->head_dim, st), st);
 }
 
+size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t max_blocks_per_seq, const pa_cache_desc* cache) {
+  if (!cache || num_seqs < 0 || max_blocks_per_seq <= 0 || cache->kv_dtype != PA_FP8_E4M3 ||
+      cache->num_kv_heads <= 0 || cache->block_size <= 0 || cache->head_dim <= 0)
+    return 0;
+  return static_cast<size_t>(
+      prefill_fp8_workspace_bytes(static_cast<int64_t>(num_seqs) * max_blocks_per_seq, cache));
+}
+
 int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_tokens,
                int32_t num_q_heads, const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
                const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens, float scale,
-               float kv_scale, pa_stream_t stream) {
+               float kv_scale, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
   int rc = check_cache(cache, k_cache, v_cache);
   if (rc) return rc;
   if (num_seqs < 0 || num_q_tokens < 1 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
@@ -627,20 +601,24 @@ int pa_prefill(void* out, const void* q, int32_t q_dtype, int32_t num_seqs, int3
   rc = check_kv_scale(cache->kv_dtype, kv_scale);
   if (rc) return rc;
   if (static_cast<int64_t>(max_blocks_per_seq) * cache->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  const bool fp8 = cache->kv_dtype == PA_FP8_E4M3;
+  if (fp8 && workspace &&
+      (!aligned16(workspace) ||
+       workspace_bytes < pa_prefill_workspace_size(num_seqs, max_blocks_per_seq, cache)))
+    return PA_ERR_WORKSPACE;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !block_tables || !context_lens || !aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
   const DecodeArgs a{out, q, q_dtype, num_seqs, num_q_heads, num_q_tokens, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, context_lens, scale, kv_scale};
-  // 16-bit caches: the head-pair kernel for an even group (head_dim 64 or
-  // 128), the one-head kernel for an odd group with head_dim 128
+  // the head-pair kernel for an even group (head_dim 64 or 128), the one-head
+  // kernel for an odd group with head_dim 128; E4M3 caches reach them through
+  // the widening pass into the caller's workspace
   const int G = num_q_heads / cache->num_kv_heads;
-  if (cache->kv_dtype != PA_FP8_E4M3 && (G % 2 == 0 || cache->head_dim == 128)) return prefill_per_head_impl(a, stream);
-  // E4M3 caches: widened, then the same kernels (an odd group with head_dim
-  // 64 stays with the packed-group kernel, which widens in shared memory)
-  if (cache->kv_dtype == PA_FP8_E4M3 && (G % 2 == 0 || cache->head_dim == 128)) {
-    const int r = prefill_fp8_widened_impl(a, stream);
-    if (r != 1) return r;
+  if (G % 2 == 0 || cache->head_dim == 128) {
+    if (!fp8) return prefill_per_head_impl(a, stream);
+    if (workspace) return prefill_fp8_widened_impl(a, workspace, stream);
   }
+  // otherwise the packed-group kernel (which widens E4M3 tiles in shared memory)
   return attn_tc_impl(a, 0, 0, nullptr, 0, stream, nullptr);
 }
 

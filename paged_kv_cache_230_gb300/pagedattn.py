@@ -30,7 +30,8 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: 
           -4: "CUDA error", -5: "out-of-range index seen by a kernel", -6: "pipeline wait timed out",
           -7: "not enough free blocks", -8: "unknown or duplicate sequence id"}
 DEVERR_BLOCK_ID, DEVERR_CONTEXT_LEN, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_LAYOUT = 0x1, 0x2, 0x4, 0x8, 0x10
-EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill", "pa_decode_split_workspace_size",
+EXPORTS = ["pa_reshape_and_cache", "pa_decode", "pa_decode_multi", "pa_prefill", "pa_prefill_workspace_size",
+           "pa_decode_split_workspace_size",
            "pa_decode_split", "pa_decode_multi_split_workspace_size", "pa_decode_multi_split", "pa_cache_and_decode",
            "pa_decode_split_noalloc", "pa_copy_blocks", "pa_gather_blocks", "pa_scatter_blocks",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append_tokens",
@@ -60,7 +61,10 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.argtypes = [P, P, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
     lib.pa_decode_multi.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32,
                                     P]
-    lib.pa_prefill.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P]
+    lib.pa_prefill.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.POINTER(CacheDesc), P, i32, P, f32, f32, P,
+                               ctypes.c_size_t, P]
+    lib.pa_prefill_workspace_size.argtypes = [i32, i32, ctypes.POINTER(CacheDesc)]
+    lib.pa_prefill_workspace_size.restype = ctypes.c_size_t
     lib.pa_prefill.restype = ctypes.c_int
     lib.pa_decode_split_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_decode_split_workspace_size.restype = ctypes.c_size_t
@@ -234,9 +238,19 @@ def decode_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_ca
     _check("pa_decode_multi", rc)
 
 
+def prefill_workspace_size(num_seqs: int, max_blocks_per_seq: int, k_cache: torch.Tensor) -> int:
+    """Bytes of the workspace prefill uses with E4M3 caches (0 for 16-bit caches)."""
+    desc = cache_desc(k_cache)
+    return int(lib.pa_prefill_workspace_size(num_seqs, max_blocks_per_seq, ctypes.byref(desc)))
+
+
 def prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float = 1.0) -> None:
-    """Chunked prefill on the tensor cores: q/out [S, C, Hq, D] (D 64 or 128), causal over the paged context."""
+            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, kv_scale: float = 1.0,
+            workspace: Optional[torch.Tensor] = None, widen: bool = True) -> None:
+    """Chunked prefill on the tensor cores: q/out [S, C, Hq, D] (D 64 or 128), causal over the paged context.
+    With E4M3 caches ``workspace`` (uint8, at least prefill_workspace_size bytes) holds the widened blocks;
+    it is allocated with torch when not given.  ``widen=False`` passes no workspace (the packed-group
+    kernel, which widens E4M3 tiles in shared memory)."""
     _check_caches(k_cache, v_cache)
     dev = k_cache.device
     _need(q, "q", (torch.float16, torch.bfloat16), 4, dev)
@@ -247,10 +261,18 @@ def prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     if out.shape != q.shape or block_tables.shape[0] != S or context_lens.shape[0] != S or D != k_cache.shape[3]:
         raise ValueError("q/out/block_tables/context_lens shapes disagree")
     desc = cache_desc(k_cache)
+    need = prefill_workspace_size(S, block_tables.shape[1], k_cache) if widen else 0
+    if not widen:
+        workspace = None
+    elif workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", device=dev)
     with torch.cuda.device(dev):
         rc = lib.pa_prefill(_ptr(out), _ptr(q), _dtype_code(q.dtype), S, C, Hq, _ptr(k_cache), _ptr(v_cache),
                             ctypes.byref(desc), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-                            float(scale), float(kv_scale), _stream(dev))
+                            float(scale), float(kv_scale), None if workspace is None else _ptr(workspace),
+                            0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(dev))
     _check("pa_prefill", rc)
 
 

@@ -221,18 +221,19 @@ def test_fp8_widened_blocks_with_nan_slots_and_bad_ids(Hq):
 
 
 def test_fp8_prefill_captured_in_a_graph_replays_the_eager_bits():
-    """The E4M3 prefill path allocates its widening scratch on the call's
-    stream from the library's pool; captured into a CUDA graph (allocation
-    and free become graph nodes) it replays the eager launch's bits."""
+    """The E4M3 prefill path (the widening pass into a workspace allocated
+    before capture, then the head-pair kernel) captured into a CUDA graph
+    replays the eager launch's bits."""
     pa = _gpu.lib()
     wl = W.make_workload(name="t", seed=48, context_lens=[300, 129, 700], Hq=8, Hkv=2, D=128, bs=16,
                          q_dtype="bf16", kv_dtype="fp8", qlen=128)
     g = _gpu.OnGpu(wl)
     g.scatter()
     out = torch.full_like(g.q, float("nan"))
+    ws = torch.empty(pa.prefill_workspace_size(wl.S, g.bt.shape[1], g.kc), dtype=torch.uint8, device="cuda")
 
     def run():
-        pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale)
+        pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale, workspace=ws)
 
     run()
     torch.cuda.synchronize()
@@ -255,3 +256,36 @@ def test_fp8_prefill_captured_in_a_graph_replays_the_eager_bits():
         torch.cuda.synchronize()
         assert pa.get_device_error() == 0
         assert torch.equal(out, eager)
+
+
+def test_fp8_workspace_contract():
+    """With E4M3 caches: no workspace takes the packed-group kernel (in-kernel
+    widening), a workspace the widening pass; both match the oracle.  A
+    workspace below pa_prefill_workspace_size, or misaligned, is refused
+    before any launch."""
+    pa = _gpu.lib()
+    wl = W.make_workload(name="t", seed=49, context_lens=[256, 700], Hq=8, Hkv=2, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype="fp8", qlen=256)
+    g = _gpu.OnGpu(wl)
+    g.scatter()
+    kc, vc = _gpu.oracle_pool(wl)
+    want = _gpu.oracle_out(wl, kc, vc)
+    need = pa.prefill_workspace_size(wl.S, g.bt.shape[1], g.kc)
+    assert need == wl.S * g.bt.shape[1] * (4 * wl.Hkv * wl.bs * wl.D + 4)
+    assert pa.prefill_workspace_size(wl.S, g.bt.shape[1], g.q.new_empty((1, 1, 1, 1))) == 0  # 16-bit caches
+    outs = []
+    for kwargs in ({"widen": False}, {"workspace": torch.empty(need, dtype=torch.uint8, device="cuda")}):
+        out = torch.full_like(g.q, float("nan"))
+        pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale, **kwargs)
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 0
+        assert _gpu.max_err(out, want) <= _gpu.tolerance(wl)
+        outs.append(out)
+    out = torch.full_like(g.q, 7.0)
+    for bad in (torch.empty(need - 16, dtype=torch.uint8, device="cuda"),
+                torch.empty(need + 32, dtype=torch.uint8, device="cuda")[1:need + 1]):
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.prefill(out, g.q, g.kc, g.vc, g.bt, g.cl, wl.scale, wl.kv_scale, workspace=bad)
+        assert e.value.status == -3
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
