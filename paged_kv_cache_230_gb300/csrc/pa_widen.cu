@@ -62,16 +62,29 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kv_kernel(const WidenPara
   if (!ok && threadIdx.x == 0) atomicOr(p.err, kErrBlockId);  // read as zeros
   const int64_t bytes = static_cast<int64_t>(p.Hkv) * p.bs * p.D;  // one block of K (or V), E4M3
   const int n16 = static_cast<int>(bytes / 16);
-  for (int i = threadIdx.x; i < 2 * n16; i += kWidenThreads) {
-    const bool v = i >= n16;
-    const int k = v ? i - n16 : i;
-    const uint8_t* src = v ? p.v_src : p.k_src;
-    const uint4 w = ok ? __ldg(reinterpret_cast<const uint4*>(src + phys * bytes) + k) : make_uint4(0u, 0u, 0u, 0u);
-    uint4 o0, o1;
-    widen16<BF16>(w, o0, o1);
-    uint4* dst = reinterpret_cast<uint4*>((v ? p.v_dst : p.k_dst) + slot * bytes) + 2 * k;
-    dst[0] = o0;
-    dst[1] = o1;
+  // four 16-byte loads in flight per thread before any store
+  for (int i0 = threadIdx.x; i0 < 2 * n16; i0 += 4 * kWidenThreads) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kWidenThreads;
+      const bool v = i >= n16;
+      const int k = v ? i - n16 : i;
+      w[u] = (ok && i < 2 * n16) ? __ldg(reinterpret_cast<const uint4*>((v ? p.v_src : p.k_src) + phys * bytes) + k)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kWidenThreads;
+      if (i >= 2 * n16) break;
+      const bool v = i >= n16;
+      const int k = v ? i - n16 : i;
+      uint4 o0, o1;
+      widen16<BF16>(w[u], o0, o1);
+      uint4* dst = reinterpret_cast<uint4*>((v ? p.v_dst : p.k_dst) + slot * bytes) + 2 * k;
+      dst[0] = o0;
+      dst[1] = o1;
+    }
   }
 }
 
