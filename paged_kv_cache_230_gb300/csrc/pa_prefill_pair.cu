@@ -9,16 +9,19 @@
 // ring, so they settle half a step apart and the tensor core runs one tile's
 // MMAs while the other tile's softmax runs.
 //
-// Tensor memory: the score tiles S_a, S_b (128 columns each) and the
-// accumulators O_a, O_b (128 columns each).  P of a tile is written as 16-bit
-// pairs over the upper 64 columns of its own S buffer (the A operand of P.V),
-// so S_x(j + 1) is issued only after P_x(j).V has completed.  16 warps:
+// A template on head_dim D (64 or 128).  Tensor memory: the score tiles S_a,
+// S_b (128 columns each) and the accumulators O_a, O_b (D columns each).  P
+// of a tile is written as 16-bit pairs over the upper 64 columns of its own S
+// buffer (the A operand of P.V), so those columns of S_x(j + 1) are issued
+// only after P_x(j).V has completed (with D = 64 its other 64 columns go out
+// as soon as the softmax has read S_x(j)).  16 warps:
 //   warps 0-3, 4-7  softmax of tile a, of tile b: one thread per row (TMEM
 //       lane), the row's 128 scores held in registers (176 a thread, by
 //       setmaxnreg), causal mask on the tiles that cross a row's position,
 //       online softmax in base 2 with a reference max that moves only by
 //       more than 2^8 (then the O row is rescaled in TMEM, where no P.V into
-//       it is in flight);
+//       it is in flight); the per-tensor E4M3 scale, when the blocks were
+//       widened from E4M3, is folded into the score scale and the output;
 //   warps 8-11  epilogue, one thread per row: O / l of both tiles to the output;
 //   warp 12     issues S_a(j) = Q_a K(j)^T, then S_b(j), each once the tile's
 //       previous P.V has completed;
