@@ -23,6 +23,8 @@ struct PrefillParams {
   int bf16;                     // 1: bf16 operands, 0: f16
   float scale_log2;             // softmax scale * log2(e)
   float vscale;                 // output factor (the E4M3 per-tensor scale; 1 for 16-bit caches)
+  int cluster;                  // two-head kernel, head_dim 128, G % 4 == 0: clusters of two CTAs
+                                // sharing each K/V tile by TMA multicast
 };
 
 // tmQ: 3-D map over q {D channels, Hq, S*C tokens}, box {64, 1, 128};

@@ -9,6 +9,13 @@
 // ring, so they settle half a step apart and the tensor core runs one tile's
 // MMAs while the other tile's softmax runs.
 //
+// With head_dim 128 on 16-bit caches and a group of four or more heads, the
+// CTAs run in clusters of two on two SMs taking the same (sequence, kv head,
+// query tile) for different head pairs: each loads every other block of a
+// K/V tile into both CTAs by TMA multicast, and each tile is released once
+// both CTAs' MMAs are done with it (commits to both), so a K/V tile crosses
+// L2 -> SM once per four query heads.
+//
 // A template on head_dim D (64 or 128).  Tensor memory: the score tiles S_a,
 // S_b (128 columns each) and the accumulators O_a, O_b (D columns each).  P
 // of a tile is written as 16-bit pairs over the upper 64 columns of its own S
@@ -156,6 +163,35 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Cluster-of-two forms (two CTAs on two SMs, sharing each K/V tile through
+// TMA multicast): this CTA's rank; a K/V box loaded into the same shared
+// memory offset of both CTAs, completing on the same-offset mbarrier of
+// each; an MMA commit arriving on the same-offset mbarrier of both CTAs;
+// both CTAs of the cluster meeting (release / acquire).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void tma_load_4d_both(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_both(uint32_t bar) {
+  const uint16_t mask = 3;
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(bar), "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // One work item.
 struct PairItem {
   int s, h, hp, qt;  // sequence, kv head, head pair of its group, query tile
@@ -169,17 +205,22 @@ struct PairItem {
 // Items run over sequences, then kv heads, then head pairs, then query tiles
 // (the last, which attends to the most tokens, first): the items that read one
 // (sequence, kv head)'s K/V are adjacent, so the CTAs running at one time share
-// a few contexts' K/V in L2.  Out of line: every warp role looks items up.
-__device__ __noinline__ PairItem pair_item(const PrefillParams& p, int idx, int nqt) {
+// a few contexts' K/V in L2.  A cluster of two (CL) takes the head pairs two
+// at a time, CTA rank hp_off the second of them.  Out of line: every warp
+// role looks items up.
+template <bool CL>
+__device__ __noinline__ PairItem pair_item(const PrefillParams& p, int idx, int nqt, int hp_off) {
   PairItem it;
-  const int per_h = (p.G / 2) * nqt;
+  constexpr int hp_per = CL ? 2 : 1;
+  const int per_h = (p.G / 2 / hp_per) * nqt;
   const int per_seq = p.Hkv * per_h;
   it.s = idx / per_seq;
   int rem = idx - it.s * per_seq;
   it.h = rem / per_h;
   rem -= it.h * per_h;
-  it.hp = rem / nqt;
-  it.qt = nqt - 1 - (rem - it.hp * nqt);
+  const int hq = rem / nqt;
+  it.hp = CL ? hq * hp_per + hp_off : hq;
+  it.qt = nqt - 1 - (rem - hq * nqt);
   const int lmax = p.maxB * p.bs;
   it.L = min(max(__ldg(p.context_lens + it.s), 0), lmax);
   it.i0 = it.qt * kRows;
@@ -190,7 +231,7 @@ __device__ __noinline__ PairItem pair_item(const PrefillParams& p, int idx, int 
   return it;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillParams p) {
@@ -211,10 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + kTmemOff);
   float* l_buf = reinterpret_cast<float*>(tail + kLOff);  // [2 tiles][128]
   const int nqt = (p.C + kRows - 1) / kRows;
-  const int total = p.S * p.Hkv * (p.G / 2) * nqt;
-  // round k of the grid: CTA c takes the c-th item, the (grid - 1 - c)-th in
-  // odd rounds (a snake, which spreads the longest items)
-  const int grid = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  // cluster form: both CTAs of cluster c take the same (sequence, kv head,
+  // query tile) items, CTA rank r head pair 2 j + r of the j-th pair of pairs
+  const int rank = CL ? static_cast<int>(cluster_rank()) : 0;
+  constexpr int hp_per = CL ? 2 : 1;
+  const int total = p.S * p.Hkv * (p.G / 2 / hp_per) * nqt;
+  // round k of the grid: CTA (cluster) c takes the c-th item, the
+  // (grid - 1 - c)-th in odd rounds (a snake, which spreads the longest items)
+  const int grid = static_cast<int>(gridDim.x) / hp_per, cta = static_cast<int>(blockIdx.x) / hp_per;
   auto item_index = [&](int k) { return k * grid + ((k & 1) ? grid - 1 - cta : cta); };
   const int rounds = total / grid;
   const int nk = rounds + (item_index(rounds) < total ? 1 : 0);
@@ -234,9 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarLReady), 2 * kRows);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
-      mbar_init(bar(kBarKEmpty + i), 1);
+      mbar_init(bar(kBarKEmpty + i), CL ? 2 : 1);  // cluster form: both CTAs' issuers
       mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarVEmpty + i), CL ? 2 : 1);
       mbar_init(bar(kBarDrain + i), 1);
     }
     *abort_flag = 0;
@@ -248,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // cluster form: the peer multicasts into this CTA's rings and arrives on
+  // its barriers only once they are initialised
+  if constexpr (CL) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto fail = [&]() {
@@ -259,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the next item with K/V tiles at or after item k of this CTA (nk if none)
   auto next_active = [&](int k, PairItem& it) -> int {
     for (; k < nk; ++k) {
-      it = pair_item(p, item_index(k), nqt);
+      it = pair_item<CL>(p, item_index(k), nqt, rank);
       if (it.ntiles > 0) return k;
     }
     return nk;
@@ -277,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // i / (D / 64) (at most 128 / 8 blocks x 2 segments = 32 boxes).
     const bool is_k = warp == 13;
     const CUtensorMap* map = is_k ? &tmK : &tmV;
-    const int my_blk = lane / Gm::kHalves, my_half = lane % Gm::kHalves;
+    // cluster form: this CTA loads every other block (rank r: blocks r, r + 2,
+    // ...) into both CTAs
+    const int my_blk = (lane / Gm::kHalves) * hp_per + rank, my_half = lane % Gm::kHalves;
     const uint32_t ring = base + (is_k ? kKOff : kVOff);
     const int full_bar = is_k ? kBarKFull : kBarVFull, empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
     if (lane == 0) {
@@ -326,8 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (my_blk < nb) {
           if (is_k && my_half == 0 && (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks))
             atomicOr(p.err, kErrBlockId);
-          tma_load_4d(ring + slot * kTileB + my_blk * p.bs * 128 + my_half * kHalf, map, full, 64 * my_half, 0, it.h,
-                      phys);
+          if constexpr (CL)
+            tma_load_4d_both(ring + slot * kTileB + my_blk * p.bs * 128 + my_half * kHalf, map, full, 64 * my_half, 0,
+                             it.h, phys);
+          else
+            tma_load_4d(ring + slot * kTileB + my_blk * p.bs * 128 + my_half * kHalf, map, full, 64 * my_half, 0,
+                        it.h, phys);
         }
       }
     }
@@ -387,7 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(bar(kBarSFull + x));
           }
           if (!ok) break;
-          tc_commit(bar(kBarKEmpty + slot));
+          if constexpr (CL)
+            tc_commit_both(bar(kBarKEmpty + slot));
+          else
+            tc_commit(bar(kBarKEmpty + slot));
           if (t == it.ntiles - 1) tc_commit(bar(kBarQEmpty));
         }
       }
@@ -453,7 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if (lane == 0) {
-          tc_commit(bar(kBarVEmpty + slot));
+          if constexpr (CL)
+            tc_commit_both(bar(kBarVEmpty + slot));
+          else
+            tc_commit(bar(kBarVEmpty + slot));
           if (t == it.ntiles - 1) tc_commit(bar(kBarOFull));
         }
         __syncwarp();
@@ -592,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ord = 0;
     bool ok = true;
     for (int k = 0; ok && k < nk; ++k) {
-      const PairItem it = pair_item(p, item_index(k), nqt);
+      const PairItem it = pair_item<CL>(p, item_index(k), nqt, rank);
       if (r == 0 && it.h == 0 && it.hp == 0 && it.qt == nqt - 1) {  // once per sequence
         const int L = __ldg(p.context_lens + it.s);
         if (L != it.L) atomicOr(p.err, kErrContextLen);  // negative, or past the table
@@ -649,16 +709,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // cluster form: neither CTA leaves while the other may still load into it
+  if constexpr (CL) cluster_sync_all();
   if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool CL>
 cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                          const CUtensorMap& tmV, int grid, cudaStream_t st) {
-  auto kern = prefill_pair_kernel<D, BF16>;
+                          const CUtensorMap& tmV, int64_t items, int nsm, cudaStream_t st) {
+  auto kern = prefill_pair_kernel<D, BF16, CL>;
   // at least half an SM's shared memory, so that no two CTAs share an SM
   // (each allocates all 512 TMEM columns; a second one would wait for them)
   constexpr int kSmemBytes = smem_bytes<D>() > 116 * 1024 ? smem_bytes<D>() : 116 * 1024;
@@ -677,8 +739,55 @@ cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tmQ, const 
   }
   if (128 * (2 * Regs<D>::kSoftmax + Regs<D>::kEpilogue + Regs<D>::kTmaMma) > regs * kThreads)
     return cudaErrorInvalidConfiguration;
-  kern<<<grid, kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if constexpr (CL) {
+    // persistent clusters of two: as many as can be resident at once (an SM
+    // left over in a GPC holds none), each taking its items in turn
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2);
+    static std::atomic<int> max_clusters[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int mc = max_clusters[dev].load(std::memory_order_relaxed);
+    if (mc == 0) {
+      e = cudaOccupancyMaxActiveClusters(&mc, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (mc <= 0) return cudaErrorInvalidConfiguration;
+      max_clusters[dev].store(mc, std::memory_order_relaxed);
+    }
+    const int64_t nc = items < mc ? items : mc;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * nc));
+  } else {
+    // persistent: one CTA per SM (all of its tensor memory)
+    cfg.gridDim = dim3(static_cast<unsigned>(items < nsm ? items : nsm));
+    cfg.numAttrs = 0;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, p);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_pair_d(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, int64_t nqt, int nsm, cudaStream_t st) {
+  // a group of four or more heads in pairs of pairs: clusters of two CTAs,
+  // each K/V tile loaded once for both (TMA multicast; head_dim 128 on
+  // 16-bit caches, where it measured level or ahead at the power cap and
+  // halves the L2 -> SM bytes)
+  if constexpr (D == 128) {
+    if (p.cluster && p.G % 4 == 0)
+      return launch_pair_t<D, BF16, true>(p, tmQ, tmK, tmV, static_cast<int64_t>(p.S) * p.Hkv * (p.G / 4) * nqt,
+                                          nsm, st);
+  }
+  return launch_pair_t<D, BF16, false>(p, tmQ, tmK, tmV, static_cast<int64_t>(p.S) * p.Hkv * (p.G / 2) * nqt, nsm,
+                                       st);
 }
 
 }  // namespace
@@ -695,13 +804,12 @@ cudaError_t launch_prefill_pair(const PrefillParams& p, const CUtensorMap& tmQ, 
     sms[dev].store(nsm, std::memory_order_relaxed);
   }
   const int64_t nqt = (p.C + kRows - 1) / kRows;
-  const int64_t total = static_cast<int64_t>(p.S) * p.Hkv * (p.G / 2) * nqt;
-  if (total > INT32_MAX) return cudaErrorInvalidValue;
-  // persistent: one CTA per SM (all of its tensor memory)
-  const int grid = static_cast<int>(total < nsm ? total : nsm);
+  if (static_cast<int64_t>(p.S) * p.Hkv * (p.G / 2) * nqt > INT32_MAX) return cudaErrorInvalidValue;
   if (p.D == 64)
-    return p.bf16 ? launch_pair_t<64, true>(p, tmQ, tmK, tmV, grid, st) : launch_pair_t<64, false>(p, tmQ, tmK, tmV, grid, st);
-  return p.bf16 ? launch_pair_t<128, true>(p, tmQ, tmK, tmV, grid, st) : launch_pair_t<128, false>(p, tmQ, tmK, tmV, grid, st);
+    return p.bf16 ? launch_pair_d<64, true>(p, tmQ, tmK, tmV, nqt, nsm, st)
+                  : launch_pair_d<64, false>(p, tmQ, tmK, tmV, nqt, nsm, st);
+  return p.bf16 ? launch_pair_d<128, true>(p, tmQ, tmK, tmV, nqt, nsm, st)
+                : launch_pair_d<128, false>(p, tmQ, tmK, tmV, nqt, nsm, st);
 }
 
 }  // namespace pa
