@@ -480,7 +480,8 @@ int prefill_fp8_widened_impl(const DecodeArgs& a, void* workspace, pa_stream_t s
   w.bs = cache->block_size;
   w.D = cache->head_dim;
   w.bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
-  if (pa::launch_widen_kv(w, st) != cudaSuccess) return finish(cudaGetLastError(), st);
+  const cudaError_t e = pa::launch_widen_kv(w, st);
+  if (e != cudaSuccess) return finish(e, st);
   pa_cache_desc wide = *cache;
   wide.kv_dtype = a.q_dtype;
   wide.num_blocks = nslot;
