@@ -126,6 +126,29 @@ __device__ __forceinline__ void mask_tokens(uint32_t (&a)[4], int lane, int n_va
   a[3] &= m_hi;
 }
 
+// Two 16x16 matrices of bytes, transposed: lanes 0-15 give the 16-byte row
+// addresses of the first, lanes 16-31 those of the second; lane (g = lane / 4,
+// c = lane % 4) receives, per matrix, column g then column g + 8 of the stored
+// rows 4c .. 4c+3 (lowest byte = row 4c).
+__device__ __forceinline__ void ldsm_b8_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                             uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// FP8 sub-tiles order their 16 tokens so that the transposing byte load of V
+// lines up with the f16 MMA: S^T row (= k index of P) r holds token
+// tok_perm(r), which puts tokens 4c .. 4c+3 at k = 2c, 2c+1, 2c+8, 2c+9.
+__device__ __forceinline__ int tok_perm(int r) { return 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3); }
+
+// Zero the E4M3 codes of tokens >= n_valid in a word holding tokens 4c .. 4c+3
+// (lowest byte first, c = lane % 4); a zero code is +0.
+__device__ __forceinline__ uint32_t token_byte_mask(int lane, int n_valid) {
+  const int nv = n_valid - 4 * (lane & 3);
+  return nv >= 4 ? 0xFFFFFFFFu : (nv <= 0 ? 0u : (1u << (8 * nv)) - 1u);
+}
+
 // Widen one lane's piece of a token row (PB bytes at a 16- or 8-byte aligned
 // shared address) to floats.
 template <int KV, int PB>
@@ -670,12 +693,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int g = (ct + nt) * 8 + 2 * qc + (e & 1);
-              int d;
-              if constexpr (KV == kE4M3) {
-                d = 16 * mt + 4 * (qr >> 1) + (qr & 1) + (e >= 2 ? 2 : 0);
-              } else {
-                d = 16 * mt + qr + (e >= 2 ? 8 : 0);
-              }
+              const int d = 16 * mt + qr + (e >= 2 ? 8 : 0);
               const float v = oacc[mt][nt][e] * ((e & 1) ? f1 : f0);
               area[g * D + d] = fst ? v : area[g * D + d] + v;
             }
@@ -730,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
               for (int nt = 0; nt < NTW; ++nt) mma16816<BF>(sacc[u][nt], a, qf[j][nt][0], qf[j][nt][1]);
             }
           } else {
-            const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int r = row0 + tok_perm((lane & 7) + ((lane >> 3) & 1) * 8);
 #pragma unroll
             for (int j = 0; j < KS; j += 2) {
               const int c = j + (lane >> 4);
@@ -757,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
           for (int u = 0; u < NSUB; ++u)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int row = 16 * u + qr + (e >= 2 ? 8 : 0);
+              const int row = 16 * u + (KV == kE4M3 ? tok_perm(qr + (e >= 2 ? 8 : 0)) : qr + (e >= 2 ? 8 : 0));
               sv[u][e] = slice0 + row < lim[nt][e & 1] ? sacc[u][nt][e] * qk_mult : -CUDART_INF_F;
             }
 #pragma unroll
@@ -813,25 +831,22 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
               for (int nt = 0; nt < NTW; ++nt) mma16816<BF>(oacc[mt][nt], a, pb[u][nt][0], pb[u][nt][1]);
             }
           } else {
-            const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            // rows = tokens, columns = channels: the transposing byte load gives
+            // lane (g, c) channels g and g + 8 of each 16-channel block at tokens
+            // 4c .. 4c+3, i.e. k = 2c, 2c+1 (low) and 2c+8, 2c+9 (high) in the
+            // sub-tile's token order
+            const int r = row0 + (lane & 15);
+            const uint32_t keep = n_valid[u] < 16 ? token_byte_mask(lane, n_valid[u]) : 0xFFFFFFFFu;
 #pragma unroll
             for (int j = 0; j < KS; j += 2) {
               const int c = j + (lane >> 4);
               uint32_t R[4];
-              ldsm_x4(vst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
+              ldsm_b8_x2_t(vst + swz<Gm>(r * Gm::BOXB + c * 16), R[0], R[1], R[2], R[3]);
 #pragma unroll
               for (int kk = 0; kk < 2; ++kk) {
-                // rows = tokens, columns = channels; transposing the widened 8x8
-                // pieces yields V^T fragments whose 16 rows are the channels
-                // 16j' + {0,1,4,5,8,9,12,13} (low) and {2,3,6,7,10,11,14,15} (high)
-                uint32_t a[4], w0, w1, w2, w3;
-                e4m3x4_to_f16x2x2(R[2 * kk], w0, w1);
-                e4m3x4_to_f16x2x2(R[2 * kk + 1], w2, w3);
-                a[0] = movm_t(w0);
-                a[1] = movm_t(w1);
-                a[2] = movm_t(w2);
-                a[3] = movm_t(w3);
-                if (n_valid[u] < 16) mask_tokens(a, lane, n_valid[u]);
+                uint32_t a[4];
+                e4m3x4_to_f16x2x2(R[2 * kk] & keep, a[0], a[2]);
+                e4m3x4_to_f16x2x2(R[2 * kk + 1] & keep, a[1], a[3]);
 #pragma unroll
                 for (int nt = 0; nt < NTW; ++nt) mma16816<false>(oacc[j + kk][nt], a, pb[u][nt][0], pb[u][nt][1]);
               }
