@@ -385,14 +385,20 @@ __device__ __forceinline__ float warp_factor(const float* ml, int w, int g) {
 
 // CTAs per SM the register budget is sized for: the 3-head shuffle variant
 // with 128 channels holds too many accumulators for three (the 16-column MMA
-// variant splits its columns over warp pairs instead).
-template <int D, bool USE_MMA, int NG>
+// variant splits its columns over warp pairs instead).  The E4M3 MMA variants
+// with 128 channels run four: their consumer warps, not the loads, bound them
+// (conversions and MMAs per byte are twice bf16's), an E4M3 stage is half the
+// bytes, so four rings fit, and the fourth CTA's warps hide more of the
+// dependent conversion -> MMA chains than the registers it costs (at most
+// 102 per thread) lose.
+template <int KV, int D, bool USE_MMA, int NG>
 constexpr int decode_min_ctas() {
+  if (KV == kE4M3 && USE_MMA && D == 128) return kMinCtasPerSm < 4 ? kMinCtasPerSm + 1 : kMinCtasPerSm;
   return (!USE_MMA && NG > 1 && D > 64) ? (kMinCtasPerSm < 2 ? kMinCtasPerSm : 2) : kMinCtasPerSm;
 }
 
 template <int KV, int D, bool USE_MMA, int NG>
-__global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
+__global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>()))
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   using Gm = Geom<KV, D>;
@@ -1014,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<D, USE_MMA, NG>()))
 template <int KV, int D, bool USE_MMA, int NG>
 int ring_stages(bool split) {
   constexpr int kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
-  constexpr int ctas = decode_min_ctas<D, USE_MMA, NG>();
+  constexpr int ctas = decode_min_ctas<KV, D, USE_MMA, NG>();
   const int budget = kSmemPerSm / ctas - kReservedPerCta;
   const int fixed = decode_smem_bytes_for<NG, D>(0, 0, split);
   int nst = (budget - fixed) / (Geom<KV, D>::STAGE_BYTES + 16);
