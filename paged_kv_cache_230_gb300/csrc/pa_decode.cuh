@@ -76,7 +76,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 // only, the run accumulator [NG][D] (last, so one-pass launches omit it).
 template <int NG, int D>
 __host__ __device__ constexpr int decode_smem_bytes_for(int ring, int nst, bool split) {
-  return 1024 + ring + NG * D * 4 + 2 * nst * 8 + kConsumerWarps * NG * 2 * 4 + 2 * NG * 2 * 4 +
+  return 1024 + ring + NG * D * 4 + 4 * nst * 8 + kConsumerWarps * NG * 2 * 4 + 2 * NG * 2 * 4 +
          (split ? NG * D * 4 : 0);
 }
 
@@ -406,6 +406,10 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
   const int RING = NST * Gm::STAGE_BYTES;
   constexpr int NCW = kConsumerWarps;
   constexpr int TILE = kTileTokens;
+  // K and V halves of a stage released separately: the 16-column MMA variant
+  // on 16-bit caches, whose consumers take longest per stage (the other
+  // variants measured faster with one barrier pair per stage)
+  constexpr bool SPLITKV = USE_MMA && NG == 16 && KV != kE4M3;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -415,11 +419,15 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
   float* qbuf = reinterpret_cast<float*>(smem + RING);
   float* area = qbuf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING + NG * D * 4);
-  float* ml = reinterpret_cast<float*>(bars + 2 * NST);  // [NCW][NG][2]
+  float* ml = reinterpret_cast<float*>(bars + 4 * NST);  // [NCW][NG][2]
   float* cml = ml + NCW * NG * 2;                         // [2][NG][2] run (m, l), double-buffered
   // [NG][D] run accumulator: split variant only (not allocated otherwise)
-  float* carea = reinterpret_cast<float*>(smem + RING + NG * D * 4 + 2 * NST * 8 + (NCW + 2) * NG * 2 * 4);
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + NST * 8;
+  float* carea = reinterpret_cast<float*>(smem + RING + NG * D * 4 + 4 * NST * 8 + (NCW + 2) * NG * 2 * 4);
+  // per stage: K (or K and V) landed, V landed, K (or K and V) free, V free.
+  // With SPLITKV the K half is released as soon as the scores are formed, so
+  // the next K streams in during the softmax and P.V of the stage
+  const uint32_t fullk0 = smem_u32(bars), fullv0 = fullk0 + NST * 8;
+  const uint32_t emptyk0 = fullv0 + NST * 8, emptyv0 = emptyk0 + NST * 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -488,8 +496,10 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, NCW);
+      mbar_init(fullk0 + 8 * i, 1);
+      mbar_init(fullv0 + 8 * i, 1);
+      mbar_init(emptyk0 + 8 * i, NCW);
+      mbar_init(emptyv0 + 8 * i, NCW);
     }
     fence_mbar_init();
   }
@@ -507,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
     const int blk_begin = tok_begin / bs;
     const int blk_end = (tok_end + bs - 1) / bs;
     const int bpt = TILE / bs;  // blocks per stage
-    const uint32_t tx = static_cast<uint32_t>(2 * bs * Gm::ROWB);
+    const uint32_t tx = static_cast<uint32_t>(bs * Gm::ROWB);  // one block of K (or V)
     int base = blk_begin;
     int cur = (base + lane < blk_end) ? __ldg(bt_row + base + lane) : -1;
     int nxt = (base + 32 + lane < blk_end) ? __ldg(bt_row + base + 32 + lane) : -1;
@@ -541,18 +551,16 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
       asm volatile("fence.proxy.async.global;" ::: "memory");
       __syncwarp();
     }
-    int t = 0;
+    int t = 0, nk = 0, nv = 0;  // tiles started; K and V halves issued
     bool ok = true;
     for (; t < ntiles; ++t) {
       const int stage = t % NST;
-      if (t >= NST && !mbar_wait(empty0 + 8 * stage, ((t / NST) - 1) & 1)) {
+      if (t >= NST && !mbar_wait(emptyk0 + 8 * stage, ((t / NST) - 1) & 1)) {
         ok = false;
         break;
       }
       const int b0 = blk_begin + t * bpt;
       const int nb = min(bpt, blk_end - b0);
-      const uint32_t full = full0 + 8 * stage;
-      if (lane == 0) mbar_arrive_expect_tx(full, tx * nb);
       const uint32_t kdst0 = ring_u32 + stage * Gm::STAGE_BYTES;
       // one lane per block of the stage (at most 64 / 8), so the warp issues
       // every block's tile loads together; issuing them from one lane after
@@ -565,21 +573,41 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
       const int rel = b0 + lane - base;  // table window index, below 64 for lane < nb
       const int pc = __shfl_sync(0xFFFFFFFFu, cur, rel & 31);
       const int pn = __shfl_sync(0xFFFFFFFFu, nxt, rel & 31);
+      const int phys = rel < 32 ? pc : pn;
+      const uint32_t kdst = kdst0 + lane * bs * Gm::BOXB;
+      const uint32_t fk = fullk0 + 8 * stage;
+      if (lane == 0) mbar_arrive_expect_tx(fk, (SPLITKV ? tx : 2 * tx) * nb);
       if (lane < nb) {
-        const int phys = rel < 32 ? pc : pn;
         if (phys < 0 || static_cast<int64_t>(phys) >= p.num_blocks) atomicOr(p.err, kErrBlockId);
-        const uint32_t kdst = kdst0 + lane * bs * Gm::BOXB;
 #pragma unroll
         for (int sg = 0; sg < Gm::NSEG; ++sg) {
-          tma_load_4d(kdst + sg * Gm::SEG_BYTES, &tmK, full, sg * Gm::BOXE, 0, h, phys);
-          tma_load_4d(kdst + Gm::HALF_BYTES + sg * Gm::SEG_BYTES, &tmV, full, sg * Gm::BOXE, 0, h, phys);
+          tma_load_4d(kdst + sg * Gm::SEG_BYTES, &tmK, fk, sg * Gm::BOXE, 0, h, phys);
+          if constexpr (!SPLITKV)
+            tma_load_4d(kdst + Gm::HALF_BYTES + sg * Gm::SEG_BYTES, &tmV, fk, sg * Gm::BOXE, 0, h, phys);
         }
+      }
+      nk = t + 1;
+      if constexpr (SPLITKV) {
+        // V half: free once the consumers have finished tile t - NST
+        if (t >= NST && !mbar_wait(emptyv0 + 8 * stage, ((t / NST) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fv = fullv0 + 8 * stage;
+        if (lane == 0) mbar_arrive_expect_tx(fv, tx * nb);
+        if (lane < nb) {
+#pragma unroll
+          for (int sg = 0; sg < Gm::NSEG; ++sg)
+            tma_load_4d(kdst + Gm::HALF_BYTES + sg * Gm::SEG_BYTES, &tmV, fv, sg * Gm::BOXE, 0, h, phys);
+        }
+        nv = t + 1;
       }
     }
     if (!ok) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       // let the copies already issued land before the CTA can exit
-      for (int u = max(0, t - NST); u < t; ++u) mbar_wait(full0 + 8 * (u % NST), (u / NST) & 1);
+      for (int u = max(0, nk - NST); u < nk; ++u) mbar_wait(fullk0 + 8 * (u % NST), (u / NST) & 1);
+      for (int u = max(0, nv - NST); u < nv; ++u) mbar_wait(fullv0 + 8 * (u % NST), (u / NST) & 1);
     }
     return;
   }
@@ -721,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
     int seg_t = 0;  // tiles done in the current segment
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % NST;
-      if (!mbar_wait(full0 + 8 * stage, (t / NST) & 1)) {
+      if (!mbar_wait(fullk0 + 8 * stage, (t / NST) & 1)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
@@ -729,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
       int n_valid[NSUB];
 #pragma unroll
       for (int u = 0; u < NSUB; ++u) n_valid[u] = min(16, tok_end - (slice0 + 16 * u));
+      bool vok = true;
       if (n_valid[0] > 0) {
         const uint32_t kst = ring_u32 + stage * Gm::STAGE_BYTES;
         const uint32_t vst = kst + Gm::HALF_BYTES;
@@ -771,6 +800,10 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
               }
             }
           }
+        }
+        if constexpr (SPLITKV) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(emptyk0 + 8 * stage);  // K read: its half may refill
         }
         // ---- online softmax over this warp's NSUB x 16 tokens ----
         uint32_t pb[NSUB][NTW][2];
@@ -820,8 +853,10 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
           }
         }
         // ---- O^T += V^T P^T, per 16-token sub-tile ----
+        if constexpr (SPLITKV) vok = __all_sync(0xFFFFFFFFu, mbar_wait(fullv0 + 8 * stage, (t / NST) & 1));
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
+          if (!vok) break;
           if (u > 0 && n_valid[u] <= 0) continue;
           const int row0 = rowbase + 16 * u;
           if constexpr (KV != kE4M3) {
@@ -859,9 +894,15 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
             }
           }
         }
+      } else if (SPLITKV && lane == 0) {
+        mbar_arrive(emptyk0 + 8 * stage);  // no rows of this warp in the tile
+      }
+      if (!vok) {
+        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        break;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (lane == 0) mbar_arrive(SPLITKV ? emptyv0 + 8 * stage : emptyk0 + 8 * stage);
       if (++seg_t == tiles_per_seg && t + 1 < ntiles) {  // a partition ends inside this CTA's run
         epilogue(t / tiles_per_seg, false);
         reset();
@@ -942,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
     int seg_t = 0;
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % NST;
-      if (!mbar_wait(full0 + 8 * stage, (t / NST) & 1)) {
+      if (!mbar_wait(fullk0 + 8 * stage, (t / NST) & 1)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
@@ -1002,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, (decode_min_ctas<KV, D, USE_MMA, NG>
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (lane == 0) mbar_arrive(emptyk0 + 8 * stage);
       if (++seg_t == tiles_per_seg && t + 1 < ntiles) {
         epilogue(t / tiles_per_seg, false);
         reset();
@@ -1023,7 +1064,7 @@ int ring_stages(bool split) {
   constexpr int ctas = decode_min_ctas<KV, D, USE_MMA, NG>();
   const int budget = kSmemPerSm / ctas - kReservedPerCta;
   const int fixed = decode_smem_bytes_for<NG, D>(0, 0, split);
-  int nst = (budget - fixed) / (Geom<KV, D>::STAGE_BYTES + 16);
+  int nst = (budget - fixed) / (Geom<KV, D>::STAGE_BYTES + 32);
   return nst < 2 ? 2 : (nst > 8 ? 8 : nst);
 }
 
