@@ -17,6 +17,7 @@ CASES = [
     (32, 32, 128, "f16", "f16", 4),    # MHA: 4 columns
     (8, 8, 64, "f16", "f16", 8),       # 8 columns
     (32, 8, 128, "bf16", "fp8", 2),    # FP8 KV
+    (32, 8, 128, "bf16", "fp8", 4),    # FP8 KV, 16 columns
     (16, 4, 64, "f16", "fp8", 4),      # FP8 rows of 64 bytes, 16 columns
     (12, 4, 128, "bf16", "bf16", 5),   # 15 columns (padded to 16)
 ]
@@ -81,3 +82,25 @@ def test_multi_token_split_decode(case, P):
     assert torch.equal(g.decode(partition_size=P), out)  # deterministic
     one_pass = g.decode().clone()
     assert _gpu.max_err(one_pass, want) <= _gpu.tolerance(wl)
+
+
+@pytest.mark.parametrize("kd", ["bf16", "fp8"])
+def test_sixteen_columns_never_read_nan_in_unused_slots(kd):
+    """16 query columns (G = 4, k = 4) over contexts whose last sub-tile is
+    ragged, with every slot outside the contexts holding NaN codes: masked
+    tokens must not reach the output, on the variant with separate K and V
+    stage barriers (16-bit caches) and on the E4M3 one."""
+    wl = W.make_workload(name="t", seed=37, context_lens=[1, 17, 33, 100, 513], Hq=32, Hkv=8, D=128, bs=16,
+                         q_dtype="bf16", kv_dtype=kd, qlen=4, fill_unused="nan")
+    g = _gpu.OnGpu(wl)
+    out = g.step()
+    torch.cuda.synchronize()
+    kc, vc = _gpu.oracle_pool(wl)
+    want = _gpu.oracle_out(wl, kc, vc)
+    assert torch.isfinite(out).all()
+    assert _gpu.max_err(out, want) <= _gpu.tolerance(wl)
+    # the split variant: 64-token partitions end inside the ragged tails too
+    out = g.decode(partition_size=64)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    assert _gpu.max_err(out, want) <= _gpu.tolerance(wl)
